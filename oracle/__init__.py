@@ -1,0 +1,148 @@
+"""fp64 CPU oracle for the DiT attention core -- TEST INFRASTRUCTURE ONLY.
+
+Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s CPU-baseline leg
+load this package.  The product path (the C-ABI library and its Python
+binding) never imports it and shares no code with it.
+
+`Oracle` wraps the plain-C library built from `oracle.c` (gcc, OpenMP, fp64,
+no fast-math, no FMA contraction).  All arrays are numpy float64; bf16 inputs
+arrive as their exact fp64 values.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+HERE = Path(__file__).resolve().parent
+SOURCE = HERE / "oracle.c"
+LIBRARY = HERE / "liboracle.so"
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.c_int64
+
+
+def build(source: Path = SOURCE, output: Path = LIBRARY, extra_flags=()) -> Path:
+    """Compile the oracle with gcc into a shared library (idempotent on mtime)."""
+    source, output = Path(source), Path(output)
+    if output.exists() and output.stat().st_mtime >= source.stat().st_mtime and not extra_flags:
+        return output
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           *extra_flags, str(source), "-o", str(output), "-lm"]
+    subprocess.run(cmd, check=True)
+    return output
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path: Path | str = LIBRARY):
+        self.path = Path(path)
+        lib = ctypes.CDLL(str(self.path))
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_rms_norm.argtypes = [_D, _D, _I64, _I64, ctypes.c_double, _D]
+        lib.oracle_rope_interleaved.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _D]
+        lib.oracle_qk_norm_rope.argtypes = [_D, _D, _D, _D, _I64, _I64, _I64, _I64, ctypes.c_double, _D]
+        lib.oracle_attention.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
+                                         _I64, _I64, ctypes.POINTER(ctypes.c_int64), _I64, _D, _D]
+        lib.oracle_attention_probs.argtypes = [_D, _D, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
+                                               _I64, _I64, _D]
+        lib.oracle_merge_lse.argtypes = [_D, _D, _I64, _I64, _I64, _I64, _I64, _D, _D]
+        for name in ("oracle_rms_norm", "oracle_rope_interleaved", "oracle_qk_norm_rope",
+                     "oracle_attention", "oracle_attention_probs", "oracle_merge_lse"):
+            getattr(lib, name).restype = None
+        self.lib = lib
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def rms_norm(self, x, w, eps: float) -> np.ndarray:
+        x = _f64(x)
+        w = _f64(w)
+        D = x.shape[-1]
+        y = np.empty_like(x)
+        self.lib.oracle_rms_norm(_ptr(x), _ptr(w), x.size // D, D, eps, _ptr(y))
+        return y
+
+    def rope_interleaved(self, x, cos, sin) -> np.ndarray:
+        """x [B, S, H, D]; cos/sin [>=S, D/2]."""
+        x = _f64(x)
+        B, S, H, D = x.shape
+        cos = _f64(cos[:S])
+        sin = _f64(sin[:S])
+        y = np.empty_like(x)
+        self.lib.oracle_rope_interleaved(_ptr(x), _ptr(cos), _ptr(sin), B, S, H, D, _ptr(y))
+        return y
+
+    def qk_norm_rope(self, x, w, cos, sin, eps: float) -> np.ndarray:
+        x = _f64(x)
+        B, S, H, D = x.shape
+        w = _f64(w)
+        cos = _f64(cos[:S])
+        sin = _f64(sin[:S])
+        y = np.empty_like(x)
+        self.lib.oracle_qk_norm_rope(_ptr(x), _ptr(w), _ptr(cos), _ptr(sin), B, S, H, D, eps, _ptr(y))
+        return y
+
+    def attention(self, q, k, v, scale: float, kv_begin: int = 0, kv_end: int | None = None, rows=None):
+        """q [B, Sq, H, D], k/v [B, Skv, H, D] -> (o [B, nrows, H, D], lse [B, H, nrows])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Sq, H, D = q.shape
+        Skv = k.shape[1]
+        kv_end = Skv if kv_end is None else kv_end
+        if rows is None:
+            nrows, rows_p = Sq, None
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            nrows, rows_p = rows.size, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+        o = np.empty((B, nrows, H, D))
+        lse = np.empty((B, H, nrows))
+        self.lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Skv, D, scale, kv_begin, kv_end,
+                                  rows_p, nrows, _ptr(o), _ptr(lse))
+        return o, lse
+
+    def attention_probs(self, q, k, scale: float, kv_begin: int = 0, kv_end: int | None = None) -> np.ndarray:
+        q, k = _f64(q), _f64(k)
+        B, Sq, H, D = q.shape
+        Skv = k.shape[1]
+        kv_end = Skv if kv_end is None else kv_end
+        p = np.empty((B, H, Sq, kv_end - kv_begin))
+        self.lib.oracle_attention_probs(_ptr(q), _ptr(k), B, H, Sq, Skv, D, scale, kv_begin, kv_end, _ptr(p))
+        return p
+
+    def merge_lse(self, o_parts, lse_parts):
+        """o_parts [C, B, Sq, H, D], lse_parts [C, B, H, Sq] -> (o [B, Sq, H, D], lse [B, H, Sq])."""
+        o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+        C, B, Sq, H, D = o_parts.shape
+        o = np.empty((B, Sq, H, D))
+        lse = np.empty((B, H, Sq))
+        self.lib.oracle_merge_lse(_ptr(o_parts), _ptr(lse_parts), C, B, H, Sq, D, _ptr(o), _ptr(lse))
+        return o, lse
+
+
+_DEFAULT: Oracle | None = None
+
+
+def get() -> Oracle:
+    """The oracle built from `oracle.c` (compiled on first use)."""
+    global _DEFAULT
+    if _DEFAULT is None:
+        build()
+        _DEFAULT = Oracle(LIBRARY)
+    return _DEFAULT
+
+
+def num_threads() -> int:
+    return get().num_threads()
+
