@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Benchmark of the DiT attention hot path on GB300.
+
+One step = the whole path on one batch of synthetic input, resident in HBM:
+QK-RMSNorm + interleaved RoPE on Q and K, flash attention over the workload's
+KV chunks (each chunk writes O_c and LSE_c), and the LSE merge.  Default
+workload: Qwen-Image joint attention (B1 H24 D128 S4312 = 256 text + 78x52
+image tokens), KV in 2 chunks.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+(the only reference this method has) on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from diffusion_transformer_attention_dit_gb300 import inputs  # noqa: E402
+
+METRIC = "attention TFLOP/s (4·B·H·Sq·Skv·D/t) and % of GB300 dense bf16 peak"
+FALLBACK_TFLOPS = 1900.0
+FALLBACK_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480": "f32", "wan720": "bf16"}
+
+
+def peaks():
+    path = ROOT / "MEASURED_PEAKS.json"
+    if path.exists():
+        try:
+            d = json.loads(path.read_text())
+            tf = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
+            gbs = d.get("hbm_gbs") or d.get("hbm_GBs")
+            if tf and gbs:
+                return float(tf), float(gbs), "measured"
+        except (ValueError, OSError):
+            pass
+    return FALLBACK_TFLOPS, FALLBACK_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) taken while the timed region runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.lines: list[str] = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [l.split(", ") for l in self.lines if l]
+        if self.uuid:
+            mine = [r for r in rows if r and self.uuid in r[0]]
+            rows = mine or rows
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle (reference arm)
+
+def oracle_step(inp, rows: np.ndarray, chunks: int):
+    """The hot path on the CPU oracle for a sample of query rows (all heads, all keys): prologue, chunked attention, merge."""
+    import oracle
+
+    orc = oracle.get()
+    w = inp.w
+    c64, s64 = inp.cos.astype(np.float64), inp.sin.astype(np.float64)
+    q = inputs.bf16_bits_to_f64(inp.q[:, rows])
+    k = inputs.bf16_bits_to_f64(inp.k)
+    v = inputs.bf16_bits_to_f64(inp.v)
+    if w.prologue:
+        q = oracle.round_bf16(orc.qk_norm_rope(q, inp.wq.astype(np.float64), c64[rows], s64[rows], w.eps))
+        k = oracle.round_bf16(orc.qk_norm_rope(k, inp.wk.astype(np.float64), c64, s64, w.eps))
+    parts = [orc.attention(q, k, v, w.scale, lo, hi) for lo, hi in w.chunk_bounds(chunks)]
+    return orc.merge_lse(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+
+
+def cpu_sample_rows(w, n: int) -> np.ndarray:
+    return np.linspace(0, w.S - 1, n).round().astype(np.int64)
+
+
+def cpu_baseline(inp, chunks: int, budget_s: float = 15.0):
+    """Time the oracle on growing row samples until about budget_s of CPU work has been measured."""
+    import oracle
+
+    w = inp.w
+    n, total_t, total_f = 16, 0.0, 0.0
+    while True:
+        rows = cpu_sample_rows(w, min(n, w.S))
+        t0 = time.perf_counter()
+        oracle_step(inp, rows, chunks)
+        dt = time.perf_counter() - t0
+        total_t += dt
+        total_f += 4.0 * w.B * w.H * len(rows) * w.S * w.D
+        if total_t >= budget_s or n >= w.S:
+            break
+        n = min(w.S, max(2 * n, int(n * budget_s / max(dt, 1e-3) / 2)))
+    return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{w.name}: prologue on all keys + attention over {chunks} KV chunks + merge for evenly spaced "
+                      f"query rows (all {w.H} heads, all {w.S} keys), row counts doubling to {len(rows)}; "
+                      f"{total_t:.1f} s of fp64 C/OpenMP work in total"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    inp = inputs.make_inputs(args.workload)
+    w = inp.w
+    chunks = args.chunks or w.chunks
+    rows = cpu_sample_rows(w, args.ref_rows)
+    for _ in range(args.warmup):
+        oracle_step(inp, rows, chunks)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(inp, rows, chunks)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.B * w.H * len(rows) * w.S * w.D * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{w.name}: {len(rows)} evenly spaced query rows per (b, h) against all {w.S} keys; prologue, "
+              f"{chunks} KV chunks and merge on the fp64 oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, chunks, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def config_of(w, chunks, args):
+    return {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "D": w.D, "Sq": w.S, "Skv": w.S,
+            "kv_chunks": chunks, "partial_o": PARTIAL[w.name], "prologue": w.prologue, "causal": False,
+            "scale": "1/sqrt(D)", "l2": "flushed before every timed step (512 MiB write)",
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from diffusion_transformer_attention_dit_gb300 import build, ops
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    ops.load_library()
+
+    inp = inputs.make_inputs(args.workload)
+    w = inp.w
+    chunks = args.chunks or w.chunks
+    pdt = torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def to_dev(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.to(dev).view(torch.bfloat16) if dtype is None else t.to(dev)
+
+    host = {"q": inp.q, "k": inp.k, "v": inp.v}
+    q, k, v = (to_dev(host[n].view(np.int16)) for n in ("q", "k", "v"))
+    wq, wk, cos, sin = (torch.from_numpy(a).to(dev) for a in (inp.wq, inp.wk, inp.cos, inp.sin))
+    B, S, H, D = w.B, w.S, w.H, w.D
+    qn, kn = torch.empty_like(q), torch.empty_like(k)
+    o_parts = torch.empty((chunks, B, S, H, D), dtype=pdt, device=dev)
+    lse_parts = torch.empty((chunks, B, H, S), dtype=torch.float32, device=dev)
+    o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    bounds = w.chunk_bounds(chunks)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches_per_step = (1 if w.prologue else 0) + chunks + (1 if chunks > 1 else 0)
+
+    def step(attn_events=None):
+        if w.prologue:
+            ops.qk_norm_rope(q, k, wq, wk, cos, sin, w.eps, q_out=qn, k_out=kn)
+            aq, ak = qn, kn
+        else:
+            aq, ak = q, k
+        if chunks == 1:
+            if attn_events is not None:
+                attn_events[0].record(stream)
+            ops.attn_fwd(aq, ak, v, None, 0, S, o=o, lse=lse)
+            if attn_events is not None:
+                attn_events[1].record(stream)
+            return
+        if attn_events is not None:
+            attn_events[0].record(stream)
+        for c, (lo, hi) in enumerate(bounds):
+            ops.attn_fwd(aq, ak, v, None, lo, hi, o=o_parts[c], lse=lse_parts[c])
+        if attn_events is not None:
+            attn_events[1].record(stream)
+        ops.attn_merge_lse(o_parts, lse_parts, o=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    ops.poll_device_error()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001
+        pass
+    step_ms, attn_ms = [], []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(uuid) as clocks:
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1, a0, a1 = ev(), ev(), ev(), ev()
+            e0.record(stream)
+            step((a0, a1))
+            e1.record(stream)
+            step_ms.append((e0, e1))
+            attn_ms.append((a0, a1))
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    ops.poll_device_error()
+    t_steps = sum(a.elapsed_time(b) for a, b in step_ms) / 1e3
+    t_attn = sum(a.elapsed_time(b) for a, b in attn_ms) / 1e3
+    t = torch.tensor([t_steps], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max = t.item()
+    flops_step = w.attention_flops()
+    value = flops_step * args.steps * world / t_max / 1e12
+
+    # end to end through the public API: pinned host inputs in, O and LSE back to pinned host memory
+    pin = {n: torch.from_numpy(np.ascontiguousarray(host[n]).view(np.int16)).pin_memory() for n in host}
+    pin_small = [torch.from_numpy(a).pin_memory() for a in (inp.wq, inp.wk, inp.cos, inp.sin)]
+    o_host = torch.empty((B, S, H, D), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    h2d = sum(t_.numel() * t_.element_size() for t_ in list(pin.values()) + pin_small)
+    d2h = o_host.numel() * 2 + lse_host.numel() * 4
+    dq, dk, dv = (torch.empty((B, S, H, D), dtype=torch.int16, device=dev) for _ in range(3))
+    dsmall = [torch.empty_like(t_, device=dev) for t_ in pin_small]
+
+    def e2e_step():
+        for src, dst in zip((pin["q"], pin["k"], pin["v"]), (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+        for src, dst in zip(pin_small, dsmall):
+            dst.copy_(src, non_blocking=True)
+        oo, ll = ops.dit_attention(dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16),
+                                   *dsmall, eps=w.eps, chunks=chunks, partial_dtype=pdt, prologue=w.prologue)
+        o_host.copy_(oo, non_blocking=True)
+        lse_host.copy_(ll, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_t = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_t += e0.elapsed_time(e1) / 1e3
+    et = torch.tensor([e2e_t], device=dev)
+    if world > 1:
+        dist.all_reduce(et, op=dist.ReduceOp.MAX)
+    e2e_value = flops_step * args.steps * world / et.item() / 1e12
+
+    if rank == 0:
+        peak_tf, peak_gbs, src = peaks()
+        achieved = flops_step * args.steps / t_attn / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, chunks, args),
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf, "peak_source": src,
+                         "traffic": args.traffic},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(inp, chunks, args.cpu_budget)
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--chunks", type=int, default=0, help="KV chunks (0: the workload's own)")
+    ap.add_argument("--ref-rows", type=int, default=48, help="query rows per (b, h) in each reference step")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per attention launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+// C ABI of the DiT attention core: argument validation, then one launcher per
+// entry point.  Declarations and the full contract are in include/ditattn.h.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/ditattn.h"
+#include "internal.h"
+
+namespace {
+
+thread_local const char *g_detail = "";
+
+dit_status fail(dit_status s, const char *why) {
+  g_detail = why;
+  return s;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte range [lo, hi) covered by a BSHD tensor with element strides {b, s, h} and contiguous D.
+struct Range {
+  uintptr_t lo, hi;
+};
+Range bshd_range(const void *p, int B, int S, int H, int D, const int64_t st[3], int esize) {
+  const int64_t last = (int64_t)(B - 1) * st[0] + (int64_t)(S - 1) * st[1] + (int64_t)(H - 1) * st[2] + D;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return {lo, lo + static_cast<uintptr_t>(last) * esize};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+dit_status from_cuda(cudaError_t e, const char *detail) {
+  if (e == cudaSuccess) return DIT_OK;
+  g_detail = detail ? detail : cudaGetErrorString(e);
+  return DIT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dit_status_string(dit_status s) {
+  switch (s) {
+    case DIT_OK: return "DIT_OK";
+    case DIT_ERR_INVALID_ARG: return "DIT_ERR_INVALID_ARG";
+    case DIT_ERR_UNSUPPORTED: return "DIT_ERR_UNSUPPORTED";
+    case DIT_ERR_CUDA: return "DIT_ERR_CUDA";
+    case DIT_ERR_TIMEOUT: return "DIT_ERR_TIMEOUT";
+  }
+  return "DIT_ERR_UNKNOWN";
+}
+
+const char *dit_last_error_detail(void) { return g_detail; }
+
+dit_status dit_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq, const float *wk,
+                            const float *cos_tab, const float *sin_tab, int B, int S, int H, int D, float eps,
+                            struct CUstream_st *stream) {
+  g_detail = "";
+  if (B < 0 || S < 0 || H < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if (D != 64 && D != 128) return fail(DIT_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  if (!(eps >= 0.f) || isinf(eps)) return fail(DIT_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if ((int64_t)B * S * H == 0) return DIT_OK;
+  if (!q || !k || !q_out || !k_out || !wq || !wk || !cos_tab || !sin_tab)
+    return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(q_out, 16) || !aligned(k_out, 16) || !aligned(cos_tab, 16) ||
+      !aligned(sin_tab, 16) || !aligned(wq, 4) || !aligned(wk, 4))
+    return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const int64_t st[3] = {(int64_t)S * H * D, (int64_t)H * D, D};
+  const Range rq = bshd_range(q, B, S, H, D, st, 2), rk = bshd_range(k, B, S, H, D, st, 2);
+  const Range rqo = bshd_range(q_out, B, S, H, D, st, 2), rko = bshd_range(k_out, B, S, H, D, st, 2);
+  if ((q_out != q && overlap(rqo, rq)) || overlap(rqo, rk) || (k_out != k && overlap(rko, rk)) || overlap(rko, rq) ||
+      overlap(rqo, rko))
+    return fail(DIT_ERR_INVALID_ARG, "outputs overlap inputs (only exact in-place is allowed)");
+  return from_cuda(ditattn::launch_qk_norm_rope(q, k, q_out, k_out, wq, wk, cos_tab, sin_tab, B, S, H, D, eps,
+                                                reinterpret_cast<cudaStream_t>(stream)),
+                   nullptr);
+}
+
+dit_status dit_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                        const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
+                        int kv_end, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                        struct CUstream_st *stream) {
+  g_detail = "";
+  if (B < 0 || H < 0 || Sq < 0 || Skv < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if (D != 64 && D != 128) return fail(DIT_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  if (o_dtype != DIT_BF16 && o_dtype != DIT_F32) return fail(DIT_ERR_INVALID_ARG, "unknown output dtype");
+  if (!(scale > 0.f) || isinf(scale)) return fail(DIT_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!q_strides || !kv_strides || !o_strides) return fail(DIT_ERR_INVALID_ARG, "null stride array");
+  if ((int64_t)B * H * Sq == 0) return DIT_OK;
+  if (kv_begin < 0 || kv_begin >= kv_end || kv_end > Skv)
+    return fail(DIT_ERR_INVALID_ARG, "key range must satisfy 0 <= kv_begin < kv_end <= Skv");
+  if (!q || !k || !v || !o || !lse) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  const int osz = o_dtype == DIT_F32 ? 4 : 2;
+  for (int i = 0; i < 3; ++i) {
+    if (q_strides[i] <= 0 || kv_strides[i] <= 0 || o_strides[i] <= 0)
+      return fail(DIT_ERR_INVALID_ARG, "strides must be positive");
+    if ((q_strides[i] * 2) % 16 || (kv_strides[i] * 2) % 16 || (o_strides[i] * osz) % 16)
+      return fail(DIT_ERR_INVALID_ARG, "byte strides must be multiples of 16");
+    if (q_strides[i] * 2 >= (int64_t(1) << 40) || kv_strides[i] * 2 >= (int64_t(1) << 40))
+      return fail(DIT_ERR_INVALID_ARG, "stride too large for a tensor map");
+  }
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const Range ro = bshd_range(o, B, Sq, H, D, o_strides, osz);
+  const Range rl = {reinterpret_cast<uintptr_t>(lse), reinterpret_cast<uintptr_t>(lse) + (uintptr_t)B * H * Sq * 4};
+  const Range rq = bshd_range(q, B, Sq, H, D, q_strides, 2);
+  const Range rk = bshd_range(k, B, Skv, H, D, kv_strides, 2), rv = bshd_range(v, B, Skv, H, D, kv_strides, 2);
+  if (overlap(ro, rq) || overlap(ro, rk) || overlap(ro, rv) || overlap(rl, rq) || overlap(rl, rk) ||
+      overlap(rl, rv) || overlap(rl, ro))
+    return fail(DIT_ERR_INVALID_ARG, "outputs overlap inputs or each other");
+  const char *detail = nullptr;
+  cudaError_t e = ditattn::launch_attn_fwd(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end,
+                                           o, o_dtype == DIT_F32, o_strides, lse,
+                                           reinterpret_cast<cudaStream_t>(stream), &detail);
+  return from_cuda(e, detail);
+}
+
+dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const float *lse_parts, int C, int B, int H,
+                              int Sq, int D, int64_t part_stride_o, int64_t part_stride_lse, void *o,
+                              dit_dtype out_dtype, float *lse, struct CUstream_st *stream) {
+  g_detail = "";
+  if (B < 0 || H < 0 || Sq < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if (C < 1) return fail(DIT_ERR_INVALID_ARG, "C must be >= 1");
+  if (D != 64 && D != 128) return fail(DIT_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+  if ((in_dtype != DIT_BF16 && in_dtype != DIT_F32) || (out_dtype != DIT_BF16 && out_dtype != DIT_F32))
+    return fail(DIT_ERR_INVALID_ARG, "unknown dtype");
+  if (!ditattn::merge_fits(C, H)) return fail(DIT_ERR_UNSUPPORTED, "C * H too large for the merge kernel");
+  if ((int64_t)B * H * Sq == 0) return DIT_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  const int isz = in_dtype == DIT_F32 ? 4 : 2, osz = out_dtype == DIT_F32 ? 4 : 2;
+  const int64_t part_o = (int64_t)B * Sq * H * D, part_l = (int64_t)B * H * Sq;
+  if (C > 1 && (part_stride_o < part_o || part_stride_lse < part_l))
+    return fail(DIT_ERR_INVALID_ARG, "part strides smaller than one part (parts would overlap)");
+  if ((part_stride_o * isz) % 16) return fail(DIT_ERR_INVALID_ARG, "part stride of O must be a multiple of 16 bytes");
+  if (!aligned(o_parts, 16) || !aligned(o, 16) || !aligned(lse_parts, 4) || !aligned(lse, 4))
+    return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const uintptr_t op = reinterpret_cast<uintptr_t>(o_parts), lp = reinterpret_cast<uintptr_t>(lse_parts);
+  const Range rin = {op, op + (uintptr_t)((C - 1) * part_stride_o + part_o) * isz};
+  const Range rlin = {lp, lp + (uintptr_t)((C - 1) * part_stride_lse + part_l) * 4};
+  const Range ro = {reinterpret_cast<uintptr_t>(o), reinterpret_cast<uintptr_t>(o) + (uintptr_t)part_o * osz};
+  const Range rl = {reinterpret_cast<uintptr_t>(lse), reinterpret_cast<uintptr_t>(lse) + (uintptr_t)part_l * 4};
+  if (overlap(ro, rin) || overlap(ro, rlin) || overlap(rl, rin) || overlap(rl, rlin) || overlap(ro, rl))
+    return fail(DIT_ERR_INVALID_ARG, "outputs overlap inputs or each other");
+  return from_cuda(ditattn::launch_merge_lse(o_parts, in_dtype == DIT_F32, lse_parts, C, B, H, Sq, D, part_stride_o,
+                                             part_stride_lse, o, out_dtype == DIT_F32, lse,
+                                             reinterpret_cast<cudaStream_t>(stream)),
+                   nullptr);
+}
+
+dit_status dit_poll_device_error(struct CUstream_st *stream) {
+  g_detail = "";
+  unsigned int v = 0;
+  cudaError_t e = ditattn::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), &v);
+  if (e != cudaSuccess) return from_cuda(e, nullptr);
+  if (v) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  return DIT_OK;
+}
+
+}  // extern "C"

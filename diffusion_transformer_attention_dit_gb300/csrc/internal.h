@@ -1,0 +1,31 @@
+// Internal launchers shared by the C-ABI translation unit and the kernel
+// translation units.  Arguments are validated by the caller (api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ditattn {
+
+// Attention forward over keys [kv_begin, kv_end).  Strides in elements {b, s, h}.
+cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                            const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
+                            void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
+                            const char **detail);
+
+cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,
+                                const float *wk, const float *cos_tab, const float *sin_tab, int B, int S, int H,
+                                int D, float eps, cudaStream_t stream);
+
+cudaError_t launch_merge_lse(const void *o_parts, bool in_f32, const float *lse_parts, int C, int B, int H, int Sq,
+                             int D, int64_t part_stride_o, int64_t part_stride_lse, void *o, bool out_f32,
+                             float *lse, cudaStream_t stream);
+
+// Largest C the merge kernel accepts, and whether C * H weights fit its shared-memory budget.
+int merge_max_parts();
+bool merge_fits(int C, int H);
+
+// Read and clear the device word in which bounded waits record that they gave up.
+cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int *value);
+
+}  // namespace ditattn

@@ -1,0 +1,181 @@
+"""Python binding of the C ABI in include/ditattn.h (argument marshalling only).
+
+Every computation runs in the CUDA kernels of libditattn.so.  PyTorch supplies
+device memory and the current stream; nothing here computes on the host and
+there is no fallback: if the library is missing or the tensors are not on a
+CUDA device, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+
+import torch
+
+LIBRARY = Path(__file__).resolve().parent / "libditattn.so"
+
+DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
+DIT_BF16, DIT_F32 = 0, 1
+EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
+            "dit_status_string", "dit_last_error_detail")
+
+_lib = None
+
+
+class DitError(RuntimeError):
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name}: {detail}" if detail else name)
+        self.status = status
+
+
+def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
+    """Load libditattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path == LIBRARY:
+        return _lib
+    path = Path(path)
+    if not path.exists():
+        raise RuntimeError(f"{path} is not built: run `python -m diffusion_transformer_attention_dit_gb300.build` "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(str(path))
+    vp, i32, i64p, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.c_float
+    lib.dit_qk_norm_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp]
+    lib.dit_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i64p, i64p, f32, i32, i32, vp, i32, i64p,
+                                 vp, vp]
+    lib.dit_attn_merge_lse.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_int64, ctypes.c_int64, vp,
+                                       i32, vp, vp]
+    lib.dit_poll_device_error.argtypes = [vp]
+    for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error"):
+        getattr(lib, name).restype = ctypes.c_int
+    lib.dit_status_string.argtypes = [ctypes.c_int]
+    lib.dit_status_string.restype = ctypes.c_char_p
+    lib.dit_last_error_detail.argtypes = []
+    lib.dit_last_error_detail.restype = ctypes.c_char_p
+    if path == LIBRARY:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != DIT_OK:
+        lib = load_library()
+        raise DitError(status, lib.dit_status_string(status).decode(), lib.dit_last_error_detail().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (there is no CPU path)")
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return DIT_BF16
+    if dt == torch.float32:
+        return DIT_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _bshd_strides(t: torch.Tensor):
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("expected a [B, S, H, D] tensor with contiguous last dim")
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def qk_norm_rope(q, k, wq, wk, cos, sin, eps: float = 1e-6, q_out=None, k_out=None, stream=None):
+    """QK-RMSNorm + interleaved RoPE.  q, k bf16 [B, S, H, D] contiguous; wq, wk fp32 [D]; cos, sin fp32 [S, D/2]."""
+    lib = load_library()
+    _cuda(q, k, wq, wk, cos, sin)
+    B, S, H, D = q.shape
+    if k.shape != q.shape or q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16:
+        raise ValueError("q and k must be bf16 tensors of the same shape")
+    if not (q.is_contiguous() and k.is_contiguous() and cos.is_contiguous() and sin.is_contiguous()):
+        raise ValueError("q, k, cos, sin must be contiguous")
+    if wq.dtype != torch.float32 or wk.dtype != torch.float32 or cos.dtype != torch.float32 or sin.dtype != torch.float32:
+        raise ValueError("weights and tables must be fp32")
+    if cos.shape[0] < S or cos.shape[-1] * 2 != D or sin.shape != cos.shape:
+        raise ValueError("cos/sin must be [>=S, D/2]")
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    k_out = torch.empty_like(k) if k_out is None else k_out
+    _check(lib.dit_qk_norm_rope(q.data_ptr(), k.data_ptr(), q_out.data_ptr(), k_out.data_ptr(), wq.data_ptr(),
+                                wk.data_ptr(), cos.data_ptr(), sin.data_ptr(), B, S, H, D, float(eps),
+                                _stream(stream)))
+    return q_out, k_out
+
+
+def attn_fwd(q, k, v, scale: float | None = None, kv_begin: int = 0, kv_end: int | None = None, o=None, lse=None,
+             o_dtype=torch.bfloat16, stream=None):
+    """Flash attention forward over keys [kv_begin, kv_end).  Returns (o [B, Sq, H, D], lse fp32 [B, H, Sq])."""
+    lib = load_library()
+    _cuda(q, k, v)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k, v must be bf16")
+    if k.stride() != v.stride():
+        raise ValueError("k and v must share strides")
+    kv_end = Skv if kv_end is None else kv_end
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if o is None:
+        o = torch.empty((B, Sq, H, D), dtype=o_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, Sq):
+        raise ValueError("lse must be contiguous fp32 [B, H, Sq]")
+    _check(lib.dit_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq, Skv, D, _bshd_strides(q),
+                            _bshd_strides(k), float(scale), int(kv_begin), int(kv_end), o.data_ptr(),
+                            _dtype_code(o.dtype), _bshd_strides(o), lse.data_ptr(), _stream(stream)))
+    return o, lse
+
+
+def attn_merge_lse(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=None, stream=None):
+    """Merge C partials: o_parts [C, B, Sq, H, D] (bf16/fp32), lse_parts fp32 [C, B, H, Sq]."""
+    lib = load_library()
+    _cuda(o_parts, lse_parts)
+    C, B, Sq, H, D = o_parts.shape
+    if tuple(lse_parts.shape) != (C, B, H, Sq) or lse_parts.dtype != torch.float32:
+        raise ValueError("lse_parts must be fp32 [C, B, H, Sq]")
+    if not (o_parts[0].is_contiguous() and lse_parts[0].is_contiguous()):
+        raise ValueError("each part must be contiguous")
+    if o is None:
+        o = torch.empty((B, Sq, H, D), dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=o_parts.device)
+    if not (o.is_contiguous() and lse.is_contiguous()):
+        raise ValueError("outputs must be contiguous")
+    _check(lib.dit_attn_merge_lse(o_parts.data_ptr(), _dtype_code(o_parts.dtype), lse_parts.data_ptr(), C, B, H, Sq,
+                                  D, o_parts.stride(0), lse_parts.stride(0), o.data_ptr(), _dtype_code(o.dtype),
+                                  lse.data_ptr(), _stream(stream)))
+    return o, lse
+
+
+def poll_device_error(stream=None):
+    """Synchronise the stream and raise DitError if a bounded device-side wait gave up since the last poll."""
+    _check(load_library().dit_poll_device_error(_stream(stream)))
+
+
+def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1, scale: float | None = None,
+                  partial_dtype=torch.float32, out_dtype=torch.bfloat16, prologue: bool = True, stream=None):
+    """The whole hot path: prologue, attention over `chunks` KV chunks, LSE merge.  Returns (o, lse)."""
+    B, S, H, D = q.shape
+    Skv = k.shape[1]
+    if prologue:
+        q, k = qk_norm_rope(q, k, wq, wk, cos, sin, eps, stream=stream)
+    if chunks == 1:
+        return attn_fwd(q, k, v, scale, o_dtype=out_dtype, stream=stream)
+    o_parts = torch.empty((chunks, B, S, H, D), dtype=partial_dtype, device=q.device)
+    lse_parts = torch.empty((chunks, B, H, S), dtype=torch.float32, device=q.device)
+    edges = [(i * Skv) // chunks for i in range(chunks + 1)]
+    for c in range(chunks):
+        attn_fwd(q, k, v, scale, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c], stream=stream)
+    return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype, stream=stream)

@@ -1,0 +1,166 @@
+/*
+ * ditattn.h -- C ABI of the DiT attention core on GB300 (sm_103a).
+ *
+ * Three operations, each one hand-written CUDA kernel launch (or a few):
+ *
+ *   dit_qk_norm_rope    per-head QK-RMSNorm + interleaved rotary embedding
+ *   dit_attn_fwd        non-causal flash attention forward -> O and fp32 LSE,
+ *                       over all keys or over one key chunk [kv_begin, kv_end)
+ *   dit_attn_merge_lse  blockwise log-sum-exp merge of per-chunk (O_c, LSE_c)
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are device pointers owned by the caller.  Activations are
+ *     [B, S, H, D] ("BSHD", element strides given where noted, last dim
+ *     contiguous), the layout a DiT block produces before the transpose to
+ *     BNSD.  LSE is fp32 [B, H, Sq], contiguous.
+ *   - bf16 means IEEE bfloat16 (stored as 16-bit words); fp32 is IEEE binary32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and allocates no device memory.  The library owns one
+ *     static device word that records a device-side wait that gave up (see
+ *     dit_poll_device_error).
+ *   - Argument errors return DIT_ERR_INVALID_ARG / DIT_ERR_UNSUPPORTED before
+ *     anything is launched.  A launch failure returns DIT_ERR_CUDA.  Work of
+ *     size zero (B, H or a sequence length 0) returns DIT_OK and launches
+ *     nothing.
+ *   - Head dim D must be 64 or 128.  Device pointers and every byte stride
+ *     must be multiples of 16 bytes (the tensor-memory-accelerator rule) unless
+ *     a function says otherwise.
+ */
+#ifndef DITATTN_H
+#define DITATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum {
+    DIT_OK = 0,
+    DIT_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad range, misalignment, aliasing */
+    DIT_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. D not 64/128) */
+    DIT_ERR_CUDA = 3,        /* CUDA runtime/driver error at launch or tensor-map creation */
+    DIT_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (reported by dit_poll_device_error) */
+} dit_status;
+
+typedef enum { DIT_BF16 = 0, DIT_F32 = 1 } dit_dtype;
+
+/*
+ * dit_qk_norm_rope -- QK-RMSNorm followed by interleaved RoPE, for Q and K in one launch.
+ *
+ * Defined by: "Cosmos Ascend NPU multi-card parallel optimisation notes",
+ * section 3.2 (RMSNorm: x * rsqrt(mean(x^2) + eps) * weight, computed in fp32)
+ * and section 3.3 (rotary embedding from precomputed cos/sin); "NPU Wan2.2-I2V
+ * model inference optimisation practice", sections "NPU rms_norm operator
+ * adaptation" and "NPU rotary_mul operator adaptation" (rotary_mode
+ * "interleave": channels 2i and 2i+1 form one rotated pair).
+ *
+ * For every (b, s, h) row x of D channels of q (weights wq) and of k (wk):
+ *   r      = 1 / sqrt(mean_d x_d^2 + eps)
+ *   y_d    = x_d * r * w_d
+ *   out_2i   = y_2i * c - y_2i+1 * s,   out_2i+1 = y_2i * s + y_2i+1 * c
+ * with c = cos_tab[s, i], s = sin_tab[s, i].  fp32 arithmetic, one rounding to
+ * bf16 at the end.  The norm is per head (over D), one weight vector shared by
+ * all heads.
+ *
+ *   q, k          bf16 [B, S, H, D], contiguous.  Read only.
+ *   q_out, k_out  bf16 [B, S, H, D], contiguous.  May equal q / k (in place);
+ *                 any other overlap is invalid.
+ *   wq, wk        fp32 [D].
+ *   cos_tab, sin_tab  fp32 [S, D/2], contiguous (shared over B and H).
+ *   eps           added to the mean square; must be >= 0.
+ * Alignment: q, k, q_out, k_out, cos_tab, sin_tab 16-byte aligned; wq, wk 4-byte.
+ */
+dit_status dit_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out,
+                            const float *wq, const float *wk, const float *cos_tab, const float *sin_tab,
+                            int B, int S, int H, int D, float eps, struct CUstream_st *stream);
+
+/*
+ * dit_attn_fwd -- non-causal multi-head flash attention forward over a key range.
+ *
+ * Defined by: "NPU Wan2.2-I2V model inference optimisation practice", section
+ * "NPU npu_fused_infer_attention_score operator adaptation" (bidirectional
+ * attention on BNSD/BSND tensors with a softmax scale, whose second output is
+ * the log-sum-exp); the key-range ("chunk") form is the per-block attention of
+ * "feat: support Ascend NPU backend (torch_npu) for Qwen-Image pipelines -
+ * #274", item 2 (ring attention over KV blocks) and of the Wan2.2 page,
+ * section "Ring Attention Overlap".
+ *
+ * For every (b, h, i), over keys j in [kv_begin, kv_end):
+ *   s_j = scale * q_i . k_j
+ *   O_i = sum_j softmax(s)_j v_j
+ *   LSE_i = ln sum_j exp(s_j)            (natural log, scale included)
+ * kv_begin = 0, kv_end = Skv is full attention.
+ *
+ *   q            bf16 [B, Sq, H, D] with element strides q_strides = {b, s, h}
+ *   k, v         bf16 [B, Skv, H, D], both with element strides kv_strides = {b, s, h}
+ *   scale        softmax scale (e.g. 1/sqrt(D)); must be finite and > 0
+ *   kv_begin, kv_end  0 <= kv_begin < kv_end <= Skv
+ *   o            [B, Sq, H, D] of o_dtype (bf16 or fp32), element strides o_strides = {b, s, h};
+ *                must not overlap q, k or v
+ *   lse          fp32 [B, H, Sq], contiguous, 4-byte aligned
+ * Strides are in elements; every stride times the element size must be a
+ * multiple of 16 bytes, and every pointer except lse 16-byte aligned.
+ * Tensor maps are built on the host per call; the kernel waits on device
+ * barriers with a bound, and a wait that gives up is reported by
+ * dit_poll_device_error (the results of that launch are then undefined).
+ */
+dit_status dit_attn_fwd(const void *q, const void *k, const void *v,
+                        int B, int H, int Sq, int Skv, int D,
+                        const int64_t q_strides[3], const int64_t kv_strides[3],
+                        float scale, int kv_begin, int kv_end,
+                        void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                        struct CUstream_st *stream);
+
+/*
+ * dit_attn_merge_lse -- merge C partial attention results over disjoint key blocks.
+ *
+ * Defined by: "feat: support Ascend NPU backend (torch_npu) for Qwen-Image
+ * pipelines - #274", item 2 (the ring loop must combine block outputs with
+ * update_out_and_lse; its default gather path avoids the precision loss of
+ * merging bf16-rounded block outputs) and "NPU Wan2.2-I2V model inference
+ * optimisation practice", section "Ring Attention Overlap" (two attention
+ * outputs combined by log-sum-exp).
+ *
+ * For every (b, h, i):
+ *   L   = m + ln sum_c exp(L_c - m),  m = max_c L_c
+ *   O   = sum_c exp(L_c - L) O_c      (fp32 accumulation)
+ * Blocks with L_c = -inf carry no weight; when every L_c is -inf, O = 0 and
+ * L = -inf.
+ *
+ *   o_parts        [C, B, Sq, H, D] of in_dtype; part c starts at
+ *                  o_parts + c * part_stride_o elements and is contiguous BSHD
+ *   lse_parts      fp32 [C, B, H, Sq]; part c at lse_parts + c * part_stride_lse
+ *   o              [B, Sq, H, D] of out_dtype, contiguous
+ *   lse            fp32 [B, H, Sq], contiguous
+ * C >= 1.  o must not overlap o_parts; lse must not overlap lse_parts.
+ * o_parts, o and part_stride_o * element size 16-byte aligned; LSE pointers
+ * 4-byte aligned.
+ */
+dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const float *lse_parts,
+                              int C, int B, int H, int Sq, int D,
+                              int64_t part_stride_o, int64_t part_stride_lse,
+                              void *o, dit_dtype out_dtype, float *lse, struct CUstream_st *stream);
+
+/*
+ * dit_poll_device_error -- synchronise `stream`, then read and clear the
+ * library's device error word.  Returns DIT_OK, DIT_ERR_TIMEOUT if a bounded
+ * device-side wait gave up since the last poll, or DIT_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+dit_status dit_poll_device_error(struct CUstream_st *stream);
+
+/* dit_status_string -- static, human-readable name of a status code (never NULL). */
+const char *dit_status_string(dit_status s);
+
+/* dit_last_error_detail -- static text describing the most recent argument or CUDA error
+ * on the calling thread ("" if none). */
+const char *dit_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DITATTN_H */

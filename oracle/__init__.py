@@ -131,6 +131,22 @@ class Oracle:
         return o, lse
 
 
+def round_bf16(x) -> np.ndarray:
+    """Round values to bfloat16 (to fp32 first, then to nearest-even bf16), returned as fp64.
+
+    The path hands bf16 tensors from one operator to the next: the RMSNorm of
+    "Cosmos Ascend NPU multi-card parallel optimisation notes", section 3.2.2,
+    returns its result in the input dtype (`.type_as(x)`), and the fused
+    attention of "NPU Wan2.2-I2V model inference optimisation practice" consumes
+    those bf16 Q/K tensors.  Composing the oracle's fp64 operators, a test
+    rounds at that boundary with this function.
+    """
+    f = np.ascontiguousarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 _DEFAULT: Oracle | None = None
 
 

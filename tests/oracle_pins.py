@@ -157,6 +157,18 @@ def pin_prologue_chain(orc):
     _close(orc.qk_norm_rope(x, w, c, s, 1e-6), ref, rtol=1e-11, atol=1e-12, what="prologue chain")
 
 
+def pin_round_bf16(orc):
+    """The op-boundary rounding matches torch's float32 -> bfloat16 conversion and exact tie cases."""
+    import oracle
+
+    rng = _rng(20)
+    x = rng.normal(0, 3, 10000).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    _close(oracle.round_bf16(x.astype(np.float64)), ref, rtol=0, atol=0, what="round_bf16 vs torch")
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(2 + 2.0 ** -7), 1 + 2.0 ** -9])
+    _close(oracle.round_bf16(ties), [1.0, 1 + 2.0 ** -6, -2.0, 1.0], rtol=0, atol=0, what="round_bf16 ties")
+
+
 # ---------------------------------------------------------------- attention
 
 def _sdpa(q, k, v, scale):

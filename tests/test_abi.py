@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+function declared in include/ditattn.h, and rejects bad arguments with a status
+code before launching anything."""
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from diffusion_transformer_attention_dit_gb300 import build, ops
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "ditattn.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load_library()
+
+
+def _declared():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^(?:const char \*|dit_status )(dit_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
+              "dit_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.dit_status_string(0) == b"DIT_OK"
+    assert lib.dit_status_string(4) == b"DIT_ERR_TIMEOUT"
+    assert lib.dit_status_string(99) == b"DIT_ERR_UNKNOWN"
+
+
+A16 = 1 << 20  # a 16-byte aligned fake device address (never dereferenced: validation fails first)
+
+
+def _st(*v):
+    return (ctypes.c_int64 * 3)(*v)
+
+
+def _attn(lib, **kw):
+    a = dict(q=A16, k=A16 * 2, v=A16 * 3, B=1, H=2, Sq=256, Skv=256, D=128, qs=_st(256 * 256, 256, 128),
+             kvs=_st(256 * 256, 256, 128), scale=0.088, lo=0, hi=256, o=A16 * 8, od=0, os=_st(256 * 256, 256, 128),
+             lse=A16 * 16, stream=None)
+    a.update(kw)
+    return lib.dit_attn_fwd(a["q"], a["k"], a["v"], a["B"], a["H"], a["Sq"], a["Skv"], a["D"], a["qs"], a["kvs"],
+                            a["scale"], a["lo"], a["hi"], a["o"], a["od"], a["os"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), ops.DIT_ERR_UNSUPPORTED),
+    (dict(q=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(q=A16 + 8), ops.DIT_ERR_INVALID_ARG),
+    (dict(lo=10, hi=10), ops.DIT_ERR_INVALID_ARG),
+    (dict(lo=0, hi=257), ops.DIT_ERR_INVALID_ARG),
+    (dict(lo=-1), ops.DIT_ERR_INVALID_ARG),
+    (dict(scale=0.0), ops.DIT_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), ops.DIT_ERR_INVALID_ARG),
+    (dict(qs=_st(256 * 256, 255, 128)), ops.DIT_ERR_INVALID_ARG),
+    (dict(od=7), ops.DIT_ERR_INVALID_ARG),
+    (dict(o=A16), ops.DIT_ERR_INVALID_ARG),          # output aliases q
+    (dict(lse=A16 * 8 + 64), ops.DIT_ERR_INVALID_ARG),  # lse inside o
+    (dict(B=-1), ops.DIT_ERR_INVALID_ARG),
+])
+def test_attn_rejects_bad_arguments(lib, kw, code):
+    assert _attn(lib, **kw) == code
+    assert lib.dit_last_error_detail() != b""
+
+
+def test_attn_empty_work_is_ok_without_launch(lib):
+    assert _attn(lib, B=0) == ops.DIT_OK
+    assert _attn(lib, Sq=0) == ops.DIT_OK
+
+
+def _prologue(lib, **kw):
+    a = dict(q=A16, k=A16 * 2, qo=A16 * 3, ko=A16 * 4, wq=A16 * 5, wk=A16 * 6, cos=A16 * 7, sin=A16 * 8, B=1, S=16,
+             H=2, D=128, eps=1e-6)
+    a.update(kw)
+    return lib.dit_qk_norm_rope(a["q"], a["k"], a["qo"], a["ko"], a["wq"], a["wk"], a["cos"], a["sin"], a["B"],
+                                a["S"], a["H"], a["D"], a["eps"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=80), ops.DIT_ERR_UNSUPPORTED),
+    (dict(cos=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(qo=A16 + 4), ops.DIT_ERR_INVALID_ARG),
+    (dict(eps=-1.0), ops.DIT_ERR_INVALID_ARG),
+    (dict(ko=A16), ops.DIT_ERR_INVALID_ARG),        # k_out overlaps q
+    (dict(qo=A16 + 1024), ops.DIT_ERR_INVALID_ARG),  # partial overlap with q
+])
+def test_prologue_rejects_bad_arguments(lib, kw, code):
+    assert _prologue(lib, **kw) == code
+
+
+def test_prologue_empty_is_ok(lib):
+    assert _prologue(lib, S=0) == ops.DIT_OK
+
+
+def _merge(lib, **kw):
+    a = dict(op=A16, idt=0, lp=A16 * 64, C=4, B=1, H=2, Sq=64, D=128, pso=64 * 2 * 128, psl=2 * 64, o=A16 * 128,
+             odt=0, lse=A16 * 160)
+    a.update(kw)
+    return lib.dit_attn_merge_lse(a["op"], a["idt"], a["lp"], a["C"], a["B"], a["H"], a["Sq"], a["D"], a["pso"],
+                                  a["psl"], a["o"], a["odt"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(C=0), ops.DIT_ERR_INVALID_ARG),
+    (dict(D=32), ops.DIT_ERR_UNSUPPORTED),
+    (dict(pso=100), ops.DIT_ERR_INVALID_ARG),
+    (dict(idt=3), ops.DIT_ERR_INVALID_ARG),
+    (dict(o=A16 + 4096), ops.DIT_ERR_INVALID_ARG),   # o inside the parts
+    (dict(C=1000), ops.DIT_ERR_UNSUPPORTED),
+])
+def test_merge_rejects_bad_arguments(lib, kw, code):
+    assert _merge(lib, **kw) == code
+
+
+def test_merge_empty_is_ok(lib):
+    assert _merge(lib, Sq=0) == ops.DIT_OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ops.attn_fwd(q, q, q)

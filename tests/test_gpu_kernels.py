@@ -1,0 +1,204 @@
+"""GPU parity of each kernel against the fp64 oracle on small seeded inputs that
+span several tiles and ragged tails (all elements compared)."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from diffusion_transformer_attention_dit_gb300 import build, inputs, ops
+from parity import (check_bf16_rounding, check_lse, check_o, dev_bf16, dev_f32, host_f64)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def vmax(v_bits) -> float:
+    return float(np.abs(inputs.bf16_bits_to_f64(v_bits)).max())
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    ops.load_library()
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+# ---------------------------------------------------------------- prologue
+
+@pytest.mark.parametrize("B,S,H,D", [(1, 256, 2, 64), (2, 37, 3, 128), (1, 129, 40, 128), (3, 5, 1, 64)])
+def test_qk_norm_rope_parity(orc, B, S, H, D):
+    q, k, _, wq, wk, cos, sin = inputs.small_case(B, S, H, D, seed=100 + S)
+    qo, ko = ops.qk_norm_rope(dev_bf16(q), dev_bf16(k), dev_f32(wq), dev_f32(wk), dev_f32(cos), dev_f32(sin), 1e-6)
+    for got, x, w in [(qo, q, wq), (ko, k, wk)]:
+        ref = orc.qk_norm_rope(inputs.bf16_bits_to_f64(x), w.astype(np.float64), cos.astype(np.float64),
+                               sin.astype(np.float64), 1e-6)
+        check_bf16_rounding(host_f64(got), ref, "prologue")
+
+
+def test_qk_norm_rope_in_place(orc):
+    q, k, _, wq, wk, cos, sin = inputs.small_case(1, 64, 4, 128, seed=7)
+    tq, tk = dev_bf16(q), dev_bf16(k)
+    ref_q, ref_k = ops.qk_norm_rope(tq, tk, dev_f32(wq), dev_f32(wk), dev_f32(cos), dev_f32(sin))
+    ops.qk_norm_rope(tq, tk, dev_f32(wq), dev_f32(wk), dev_f32(cos), dev_f32(sin), q_out=tq, k_out=tk)
+    assert torch.equal(tq, ref_q) and torch.equal(tk, ref_k)
+
+
+# ---------------------------------------------------------------- attention
+
+SHAPES = [
+    # B, H, Sq, Skv, D
+    (1, 2, 256, 256, 64),
+    (1, 2, 256, 256, 128),
+    (2, 3, 200, 333, 128),
+    (1, 1, 1, 1, 128),
+    (1, 2, 1, 700, 64),
+    (1, 1, 517, 3, 128),
+    (2, 2, 300, 129, 64),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,D", SHAPES)
+@pytest.mark.parametrize("o_dtype", ["bf16", "f32"])
+def test_attn_fwd_full_parity(orc, B, H, Sq, Skv, D, o_dtype):
+    q, k, v, *_ = inputs.small_case(B, Sq, H, D, seed=Sq * 7 + Skv, Skv=Skv)
+    dt = torch.bfloat16 if o_dtype == "bf16" else torch.float32
+    scale = 1.0 / math.sqrt(D)
+    o, lse = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v), scale, o_dtype=dt)
+    ro, rl = orc.attention(inputs.bf16_bits_to_f64(q), inputs.bf16_bits_to_f64(k), inputs.bf16_bits_to_f64(v), scale)
+    check_o(host_f64(o), ro, f32=o_dtype == "f32", what=f"attn {B, H, Sq, Skv, D}", vmax=vmax(v))
+    check_lse(host_f64(lse), rl, what=f"attn {B, H, Sq, Skv, D}")
+
+
+@pytest.mark.parametrize("lo,hi", [(0, 64), (64, 128), (5, 6), (100, 333), (0, 333), (129, 300)])
+def test_attn_fwd_chunk_parity(orc, lo, hi):
+    B, H, Sq, Skv, D = 2, 2, 150, 333, 128
+    q, k, v, *_ = inputs.small_case(B, Sq, H, D, seed=31, Skv=Skv, k_std=2.0)
+    o, lse = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v), 0.1, lo, hi, o_dtype=torch.float32)
+    ro, rl = orc.attention(inputs.bf16_bits_to_f64(q), inputs.bf16_bits_to_f64(k), inputs.bf16_bits_to_f64(v), 0.1,
+                           lo, hi)
+    check_o(host_f64(o), ro, f32=True, what=f"chunk [{lo},{hi})", vmax=vmax(v[:, lo:hi]))
+    check_lse(host_f64(lse), rl, what=f"chunk [{lo},{hi})")
+
+
+def test_attn_fwd_strided_views(orc):
+    """q/k/v as views into a packed [B, S, 3, H, D] QKV buffer and O into a wider buffer."""
+    B, S, H, D = 1, 190, 3, 64
+    bits = inputs.bf16_normal(B * S * 3 * H * D, seed=44).reshape(B, S, 3, H, D)
+    qkv = dev_bf16(bits)
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    o_buf = torch.zeros((B, S, H, 2 * D), dtype=torch.bfloat16, device="cuda")
+    o = o_buf[..., :D]
+    _, lse = ops.attn_fwd(q, k, v, 0.125, o=o)
+    f = inputs.bf16_bits_to_f64(bits)
+    ro, rl = orc.attention(f[:, :, 0], f[:, :, 1], f[:, :, 2], 0.125)
+    check_o(host_f64(o), ro, what="strided")
+    check_lse(host_f64(lse), rl, what="strided")
+    assert torch.count_nonzero(o_buf[..., D:]) == 0, "kernel wrote outside the O view"
+
+
+def test_attn_fwd_deterministic():
+    q, k, v, *_ = inputs.small_case(1, 300, 4, 128, seed=9)
+    args = [dev_bf16(q), dev_bf16(k), dev_bf16(v)]
+    o1, l1 = ops.attn_fwd(*args)
+    o2, l2 = ops.attn_fwd(*args)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_attn_fwd_sharp_softmax_rescale(orc):
+    """Large logits (K x 8) make the running max grow between blocks: exercises the O rescale path."""
+    B, H, S, D = 1, 2, 640, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=77, k_std=8.0)
+    o, lse = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v), 1 / math.sqrt(D), o_dtype=torch.float32)
+    ro, rl = orc.attention(inputs.bf16_bits_to_f64(q), inputs.bf16_bits_to_f64(k), inputs.bf16_bits_to_f64(v),
+                           1 / math.sqrt(D))
+    check_o(host_f64(o), ro, f32=True, what="sharp", vmax=vmax(v))
+    check_lse(host_f64(lse), rl, what="sharp")
+
+
+# ---------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("C", [1, 2, 3, 8])
+@pytest.mark.parametrize("in_dt,out_dt", [("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16"), ("bf16", "f32")])
+def test_merge_parity(orc, C, in_dt, out_dt):
+    B, Sq, H, D = 2, 77, 3, 128
+    rng = np.random.default_rng(C)
+    dts = {"bf16": torch.bfloat16, "f32": torch.float32}
+    o_parts = torch.from_numpy(rng.normal(0, 1, (C, B, Sq, H, D)).astype(np.float32)).cuda().to(dts[in_dt])
+    lse_np = rng.normal(3, 2, (C, B, H, Sq)).astype(np.float32)
+    lse_np[0, 0, 0, :5] = -np.inf          # an empty block for a few rows
+    if C > 1:
+        lse_np[:, 1, 2, 7] = -np.inf       # every block empty for one row
+    lse_parts = torch.from_numpy(lse_np).cuda()
+    o, lse = ops.attn_merge_lse(o_parts, lse_parts, out_dtype=dts[out_dt])
+    ro, rl = orc.merge_lse(host_f64(o_parts), lse_np.astype(np.float64))
+    got_o, got_l = host_f64(o), host_f64(lse)
+    finite = np.isfinite(rl)
+    assert np.array_equal(finite, np.isfinite(got_l))
+    np.testing.assert_allclose(got_l[finite], rl[finite], rtol=0, atol=2e-6 * (1 + np.abs(rl[finite]).max()))
+    if out_dt == "f32":
+        np.testing.assert_allclose(got_o, ro, rtol=1e-5, atol=1e-5)
+    else:
+        check_bf16_rounding(got_o, ro, "merge")
+    if C > 1:
+        assert np.all(got_o[1, 7, 2] == 0)
+
+
+@pytest.mark.parametrize("C,partial", [(2, "f32"), (4, "bf16"), (4, "f32"), (7, "f32")])
+def test_chunked_merged_equals_full(orc, C, partial):
+    """chunk-mode attention over C key blocks merged by LSE == single-pass attention (and the oracle)."""
+    B, H, S, D = 1, 3, 500, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=C * 11, k_std=3.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    dt = torch.float32 if partial == "f32" else torch.bfloat16
+    edges = [(i * S) // C for i in range(C + 1)]
+    o_parts = torch.empty((C, B, S, H, D), dtype=dt, device="cuda")
+    lse_parts = torch.empty((C, B, H, S), dtype=torch.float32, device="cuda")
+    for c in range(C):
+        ops.attn_fwd(tq, tk, tv, None, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c])
+    om, lm = ops.attn_merge_lse(o_parts, lse_parts, out_dtype=torch.bfloat16)
+    of, lf = ops.attn_fwd(tq, tk, tv)
+    ro, rl = orc.attention(inputs.bf16_bits_to_f64(q), inputs.bf16_bits_to_f64(k), inputs.bf16_bits_to_f64(v),
+                           1 / math.sqrt(D))
+    check_o(host_f64(om), ro, what="merged vs oracle")
+    check_lse(host_f64(lm), rl, what="merged vs oracle")
+    check_o(host_f64(om), host_f64(of), what="merged vs single pass")
+    check_lse(host_f64(lm), host_f64(lf), what="merged vs single pass")
+    # a ring loop that never merges returns one block's own output: make sure we do not
+    for c in range(C):
+        assert (host_f64(om) - host_f64(o_parts[c])).__abs__().max() > 0.05
+
+
+def test_poll_device_error_clean():
+    q, k, v, *_ = inputs.small_case(1, 128, 1, 64, seed=3)
+    ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v))
+    ops.poll_device_error()
+
+
+def test_full_hot_path_tiny(orc):
+    """Prologue + 4 KV chunks + merge on the tiny workload, bf16 and fp32 outputs."""
+    inp = inputs.make_inputs("tiny")
+    w = inp.w
+    dq = dev_bf16(inp.q)
+    dk = dev_bf16(inp.k)
+    dv = dev_bf16(inp.v)
+    args = (dev_f32(inp.wq), dev_f32(inp.wk), dev_f32(inp.cos), dev_f32(inp.sin))
+    f = {n: inputs.bf16_bits_to_f64(getattr(inp, n)) for n in ("q", "k", "v")}
+    # the prologue hands bf16 Q/K to attention, so the oracle chain rounds there too
+    rq = oracle.round_bf16(orc.qk_norm_rope(f["q"], inp.wq.astype(np.float64), inp.cos.astype(np.float64),
+                                            inp.sin.astype(np.float64), w.eps))
+    rk = oracle.round_bf16(orc.qk_norm_rope(f["k"], inp.wk.astype(np.float64), inp.cos.astype(np.float64),
+                                            inp.sin.astype(np.float64), w.eps))
+    parts = [orc.attention(rq, rk, f["v"], w.scale, lo, hi) for lo, hi in w.chunk_bounds()]
+    ro, rl = orc.merge_lse(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    for out_dt, part_dt in [(torch.bfloat16, torch.bfloat16), (torch.float32, torch.float32)]:
+        o, lse = ops.dit_attention(dq, dk, dv, *args, eps=w.eps, chunks=w.chunks, partial_dtype=part_dt,
+                                   out_dtype=out_dt)
+        check_o(host_f64(o), ro, f32=out_dt == torch.float32, what="tiny hot path", vmax=vmax(inp.v))
+        check_lse(host_f64(lse), rl, what="tiny hot path")
