@@ -257,6 +257,15 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     ops.poll_device_error()
+    if not args.steps:
+        # enough steps for about 2 s of timed work (so the clock sampler sees the region)
+        e0, e1 = ev(), ev()
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        args.steps = int(min(4000, max(10, 2000.0 / max(e0.elapsed_time(e1), 1e-3))))
 
     uuid = None
     try:
@@ -354,7 +363,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s worth)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
@@ -367,6 +376,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    elif not args.steps:
+        args.steps = 5
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -266,9 +266,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-      float mx = s[0];
+      // row max as 8 independent chains and a tree (a single chain is ~127 dependent fmax)
+      float mp[8];
 #pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      for (int u = 0; u < 8; ++u) mp[u] = s[u];
+#pragma unroll
+      for (int i = 8; i < kBN; i += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mp[u] = fmaxf(mp[u], s[i + u]);
+      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       mx *= sl2;
       if (j == 0) {
         m = mx;
@@ -290,21 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       const float nm = -m;
-      float rs = 0.f;
+      float rp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // row-sum partials (independent chains)
       uint32_t p0[32], p1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float a = ex2(fmaf(s[2 * i], sl2, nm)), c = ex2(fmaf(s[2 * i + 1], sl2, nm));
-        rs += a + c;
+        rp[i & 7] += a + c;
         p0[i] = pack_bf16(a, c);
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float a = ex2(fmaf(s[64 + 2 * i], sl2, nm)), c = ex2(fmaf(s[64 + 2 * i + 1], sl2, nm));
-        rs += a + c;
+        rp[i & 7] += a + c;
         p1[i] = pack_bf16(a, c);
       }
-      l += rs;
+      l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       tmem_st_x32(tS, p0);
       tmem_st_x32(tS + 32, p1);
       tmem_st_wait();

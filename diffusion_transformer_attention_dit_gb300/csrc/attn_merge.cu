@@ -7,12 +7,13 @@
 // every (b, h, i):
 //   L = m + ln sum_c exp(L_c - m),  m = max_c L_c;   O = sum_c exp(L_c - L) O_c
 //
-// HBM-bound: C partial rows in, one row out.  A CTA owns TQ consecutive query
-// rows of one batch for all heads.  Phase 1 turns the C partial LSEs of each
-// (h, i) into weights in shared memory (LSE reads are contiguous in i) and
-// writes the merged LSE.  Phase 2 streams the O partials as 16-byte vectors,
-// all C loads of a vector issued before the fp32 accumulation, and writes the
-// merged row.
+// HBM-bound: C partial rows in, one row out.  The O tensors are contiguous
+// BSHD, so rows (b, i, h) are consecutive D-element runs; each row is spread
+// over D/N lanes holding one 16-byte vector (N elements) each, and a CTA
+// covers 256/(D/N) consecutive rows.  Every lane of a row reads the same C
+// partial LSEs (one broadcast transaction each), forms the weights in fp32,
+// issues up to 4 partial loads before accumulating, and writes its vector of
+// the merged row; lane 0 of the row writes the merged LSE.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,21 +25,10 @@ namespace ditattn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxC = 64;
-constexpr int kSmemBudget = 48 * 1024;
+constexpr int kMaxC = 1024;
+constexpr int kGroup = 4;  // partial loads in flight per lane (x the CTAs resident per SM)
 
-template <typename T>
-struct Vec;
-template <>
-struct Vec<float> {
-  static constexpr int N = 4;
-};
-template <>
-struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-};
-
-__device__ __forceinline__ void load_vec(const float *p, float (&v)[8]) {
+__device__ __forceinline__ void load_vec(const float *p, float (&v)[4]) {
   const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
   v[0] = a.x;
   v[1] = a.y;
@@ -62,119 +52,105 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 template <int N>
 __device__ __forceinline__ void store_vec(float *p, const float (&v)[8]) {
-  if (N == 4) {
-    *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
-  } else {
-    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-  }
+  reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  if (N == 8) reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 template <int N>
 __device__ __forceinline__ void store_vec(__nv_bfloat16 *p, const float (&v)[8]) {
-  if (N == 4) {
+  if (N == 4)
     *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
-  } else {
+  else
     *reinterpret_cast<uint4 *>(p) =
         make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
-  }
 }
 
-template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(kThreads) merge_lse_kernel(const Tin *__restrict__ o_parts,
+template <typename Tin, typename Tout, int D>
+__global__ void __launch_bounds__(kThreads, 4) merge_lse_kernel(const Tin *__restrict__ o_parts,
                                                              const float *__restrict__ lse_parts, int C, int H,
-                                                             int Sq, int D, long long pso, long long psl, Tout *o,
-                                                             float *lse, int TQ) {
-  extern __shared__ float wgt[];  // [TQ][H][C]
-  const int b = blockIdx.y;
-  const int q0 = blockIdx.x * TQ;
-  const int nq = min(TQ, Sq - q0);
+                                                             int Sq, long long n_rows, long long pso, long long psl,
+                                                             Tout *o, float *lse) {
+  constexpr int N = 16 / sizeof(Tin);  // elements per 16-byte vector
+  constexpr int kLanes = D / N;        // lanes per row
+  constexpr int kRows = kThreads / kLanes;
+  const long long row = (long long)blockIdx.x * kRows + threadIdx.x / kLanes;
+  const int lane = threadIdx.x % kLanes;
+  if (row >= n_rows) return;
+  const int h = static_cast<int>(row % H);
+  const long long bq = row / H;
+  const long long q = bq % Sq, b = bq / Sq;
+  const long long li = (b * H + h) * Sq + q;
+  const long long off = row * D + (long long)lane * N;
 
-  for (int idx = threadIdx.x; idx < H * TQ; idx += kThreads) {
-    const int h = idx / TQ, qq = idx % TQ;
-    if (qq >= nq) continue;
-    const long long li = ((long long)b * H + h) * Sq + q0 + qq;
-    float mx = -INFINITY;
-    for (int c = 0; c < C; ++c) mx = fmaxf(mx, lse_parts[c * psl + li]);
-    float *w = wgt + ((long long)qq * H + h) * C;
-    if (mx == -INFINITY) {
-      for (int c = 0; c < C; ++c) w[c] = 0.f;
-      lse[li] = -INFINITY;
-    } else {
-      float sum = 0.f;
-      for (int c = 0; c < C; ++c) sum += expf(lse_parts[c * psl + li] - mx);
-      const float L = mx + logf(sum);
-      for (int c = 0; c < C; ++c) w[c] = expf(lse_parts[c * psl + li] - L);
-      lse[li] = L;
-    }
+  float mx = -INFINITY;
+  for (int c = 0; c < C; ++c) mx = fmaxf(mx, lse_parts[c * psl + li]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (mx == -INFINITY) {  // no block holds any key for this row
+    store_vec<N>(o + off, acc);
+    if (lane == 0) lse[li] = -INFINITY;
+    return;
   }
-  __syncthreads();
-
-  constexpr int N = Vec<Tin>::N;
-  const int vpr = D / N;  // vectors per row
-  const long long row0 = ((long long)b * Sq + q0) * H;
-  const int items = nq * H * vpr;
-  for (int it = threadIdx.x; it < items; it += kThreads) {
-    const int rh = it / vpr, dv = it % vpr;  // rh = qq * H + h
-    const long long off = (row0 + rh) * D + (long long)dv * N;
-    const float *w = wgt + (long long)rh * C;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int c = 0;
-    for (; c + 4 <= C; c += 4) {
-      float v0[8], v1[8], v2[8], v3[8];
-      load_vec(o_parts + c * pso + off, v0);
-      load_vec(o_parts + (c + 1) * pso + off, v1);
-      load_vec(o_parts + (c + 2) * pso + off, v2);
-      load_vec(o_parts + (c + 3) * pso + off, v3);
+  float sum = 0.f;
+  for (int c = 0; c < C; ++c) sum += expf(lse_parts[c * psl + li] - mx);
+  const float L = mx + logf(sum);
+  for (int c0 = 0; c0 < C; c0 += kGroup) {
+    float v[kGroup][N], w[kGroup];
 #pragma unroll
-      for (int i = 0; i < N; ++i) {
-        acc[i] = fmaf(w[c], v0[i], acc[i]);
-        acc[i] = fmaf(w[c + 1], v1[i], acc[i]);
-        acc[i] = fmaf(w[c + 2], v2[i], acc[i]);
-        acc[i] = fmaf(w[c + 3], v3[i], acc[i]);
+    for (int u = 0; u < kGroup; ++u) {
+      if (c0 + u < C) {
+        load_vec(o_parts + (c0 + u) * pso + off, v[u]);
+        w[u] = expf(lse_parts[(c0 + u) * psl + li] - L);
       }
     }
-    for (; c < C; ++c) {
-      float v0[8];
-      load_vec(o_parts + c * pso + off, v0);
 #pragma unroll
-      for (int i = 0; i < N; ++i) acc[i] = fmaf(w[c], v0[i], acc[i]);
+    for (int u = 0; u < kGroup; ++u) {
+      if (c0 + u < C) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+      }
     }
-    store_vec<N>(o + off, acc);
   }
+  store_vec<N>(o + off, acc);
+  if (lane == 0) lse[li] = L;
+}
+
+template <typename Tin, typename Tout, int D>
+cudaError_t launch_typed(const void *o_parts, const float *lse_parts, int C, int B, int H, int Sq, long long pso,
+                         long long psl, void *o, float *lse, cudaStream_t stream) {
+  constexpr int kRows = kThreads / (D / (16 / sizeof(Tin)));
+  const long long n_rows = (long long)B * Sq * H;
+  const long long blocks = (n_rows + kRows - 1) / kRows;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  merge_lse_kernel<Tin, Tout, D><<<(unsigned)blocks, kThreads, 0, stream>>>(
+      static_cast<const Tin *>(o_parts), lse_parts, C, H, Sq, n_rows, pso, psl, static_cast<Tout *>(o), lse);
+  return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
-cudaError_t launch_typed(const void *o_parts, const float *lse_parts, int C, int B, int H, int Sq, int D,
-                         long long pso, long long psl, void *o, float *lse, cudaStream_t stream) {
-  int TQ = 32;
-  while (TQ > 1 && (long long)TQ * H * C * 4 > kSmemBudget) TQ >>= 1;
-  const size_t smem = (size_t)TQ * H * C * 4;
-  dim3 grid((Sq + TQ - 1) / TQ, B);
-  merge_lse_kernel<Tin, Tout><<<grid, kThreads, smem, stream>>>(static_cast<const Tin *>(o_parts), lse_parts, C, H,
-                                                                Sq, D, pso, psl, static_cast<Tout *>(o), lse, TQ);
-  return cudaGetLastError();
+cudaError_t launch_d(const void *o_parts, const float *lse_parts, int C, int B, int H, int Sq, int D, long long pso,
+                     long long psl, void *o, float *lse, cudaStream_t stream) {
+  if (D == 64) return launch_typed<Tin, Tout, 64>(o_parts, lse_parts, C, B, H, Sq, pso, psl, o, lse, stream);
+  return launch_typed<Tin, Tout, 128>(o_parts, lse_parts, C, B, H, Sq, pso, psl, o, lse, stream);
 }
 
 }  // namespace
 
 int merge_max_parts() { return kMaxC; }
 
-bool merge_fits(int C, int H) { return C <= kMaxC && (long long)H * C * 4 <= kSmemBudget; }
+bool merge_fits(int C, int H) { return C <= kMaxC && H >= 1; }
 
 cudaError_t launch_merge_lse(const void *o_parts, bool in_f32, const float *lse_parts, int C, int B, int H, int Sq,
                              int D, int64_t part_stride_o, int64_t part_stride_lse, void *o, bool out_f32,
                              float *lse, cudaStream_t stream) {
   if (in_f32 && out_f32)
-    return launch_typed<float, float>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse, o, lse,
-                                      stream);
+    return launch_d<float, float>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse, o, lse, stream);
   if (in_f32)
-    return launch_typed<float, __nv_bfloat16>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse, o,
-                                              lse, stream);
+    return launch_d<float, __nv_bfloat16>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse, o, lse,
+                                          stream);
   if (out_f32)
-    return launch_typed<__nv_bfloat16, float>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse, o,
-                                              lse, stream);
-  return launch_typed<__nv_bfloat16, __nv_bfloat16>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o,
-                                                    part_stride_lse, o, lse, stream);
+    return launch_d<__nv_bfloat16, float>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse, o, lse,
+                                          stream);
+  return launch_d<__nv_bfloat16, __nv_bfloat16>(o_parts, lse_parts, C, B, H, Sq, D, part_stride_o, part_stride_lse,
+                                                o, lse, stream);
 }
 
 }  // namespace ditattn

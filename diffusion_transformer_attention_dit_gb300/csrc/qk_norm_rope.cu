@@ -113,10 +113,8 @@ cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void 
                                 const float *wk, const float *cos_tab, const float *sin_tab, int B, int S, int H,
                                 int D, float eps, cudaStream_t stream) {
   const long long n_pos = (long long)B * S;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long blocks = n_pos < (long long)sms * 16 ? n_pos : (long long)sms * 16;
+  // one CTA per sequence position while the grid fits; grid-stride beyond that
+  const long long blocks = n_pos < 0x7fffffffLL ? n_pos : 0x7fffffffLL;
   if (D == 64)
     qk_norm_rope_kernel<64><<<(unsigned)blocks, kThreads, 0, stream>>>(
         static_cast<const uint4 *>(q), static_cast<const uint4 *>(k), static_cast<uint4 *>(q_out),

@@ -122,7 +122,7 @@ def _merge(lib, **kw):
     (dict(pso=100), ops.DIT_ERR_INVALID_ARG),
     (dict(idt=3), ops.DIT_ERR_INVALID_ARG),
     (dict(o=A16 + 4096), ops.DIT_ERR_INVALID_ARG),   # o inside the parts
-    (dict(C=1000), ops.DIT_ERR_UNSUPPORTED),
+    (dict(C=5000), ops.DIT_ERR_UNSUPPORTED),
 ])
 def test_merge_rejects_bad_arguments(lib, kw, code):
     assert _merge(lib, **kw) == code
