@@ -17,10 +17,13 @@
 //               tile's work while the other tile's softmax runs.
 //   warps 0-7   two softmax warpgroups, one per query tile; thread = one query
 //               row (TMEM lane), so row max / row sum need no shuffles.  Online
-//               softmax in base 2 with the scale folded into one FFMA; the O
-//               rescale is lazy (only when a row max grows by more than 2^8),
-//               exact after the final 1/l.  P is written back over S in TMEM
-//               as bf16.  Epilogue: O / l from TMEM to global, LSE = (m + log2 l) ln 2.
+//               softmax in base 2: the scale is folded into one packed FFMA2 per
+//               pair of scores, row sums use packed FADD2 and the row max a
+//               3-input max; the O rescale is lazy (only when a row max grows by
+//               more than 2^8), exact after the final 1/l.  P is written back
+//               over S in TMEM as bf16.  Epilogue: O / l from TMEM, staged in
+//               the idle Q buffer in swizzled layout and written by TMA;
+//               LSE = (m + log2 l) ln 2.
 // TMEM (512 columns): S/P of tile 0 | S/P of tile 1 | O of tile 0 | O of tile 1.
 // Every mbarrier wait is bounded (about 2 s); a wait that gives up sets the
 // library's device error word and the CTA drains its in-flight copies and MMAs,
@@ -97,6 +100,37 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed pairs of fp32 (one 64-bit register pair) for the FFMA2 / FADD2 / FMUL2 pipes.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -105,7 +139,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnArgs args) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const AttnArgs args) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -144,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tm_q);
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
+    tma_prefetch_map(&tm_o);
   }
   if (warp == kWarpMma) {
     tmem_alloc(base + L::kTmemSlot, kTmemCols);
@@ -249,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_base + t * kBN;
     const uint32_t tO = tmem + lane_base + L::kTmemO + t * D;
     const float sl2 = args.scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
@@ -266,16 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-      // row max as 8 independent chains and a tree (a single chain is ~127 dependent fmax)
-      float mp[8];
+        // row max: 3-input max over 4 independent chains, then a tree
+      float mp[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mp[u] = s[u];
+      for (int i = 4; i < kBN - 4; i += 8)
 #pragma unroll
-      for (int i = 8; i < kBN; i += 8)
+        for (int u = 0; u < 4; ++u) mp[u] = max3(mp[u], s[i + u], s[i + 4 + u]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mp[u] = fmaxf(mp[u], s[i + u]);
-      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      mx *= sl2;
+      for (int u = 0; u < 4; ++u) mp[u] = fmaxf(mp[u], s[kBN - 4 + u]);
+      const float mx = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])) * sl2;
       if (j == 0) {
         m = mx;
       } else if (__any_sync(0xffffffffu, mx > m + kRescaleLog2)) {
@@ -295,61 +331,102 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      const float nm = -m;
-      float rp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // row-sum partials (independent chains)
+const uint64_t nm2 = f2(-m, -m);
+      uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};  // packed row-sum partials (0.0f bit patterns)
       uint32_t p0[32], p1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float a = ex2(fmaf(s[2 * i], sl2, nm)), c = ex2(fmaf(s[2 * i + 1], sl2, nm));
-        rp[i & 7] += a + c;
+        float a, c;
+        f2_split(f2_fma(f2(s[2 * i], s[2 * i + 1]), sl2x2, nm2), a, c);
+        a = ex2(a);
+        c = ex2(c);
+        rs[i & 3] = f2_add(rs[i & 3], f2(a, c));
         p0[i] = pack_bf16(a, c);
       }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float a = ex2(fmaf(s[64 + 2 * i], sl2, nm)), c = ex2(fmaf(s[64 + 2 * i + 1], sl2, nm));
-        rp[i & 7] += a + c;
+        float a, c;
+        f2_split(f2_fma(f2(s[64 + 2 * i], s[64 + 2 * i + 1]), sl2x2, nm2), a, c);
+        a = ex2(a);
+        c = ex2(c);
+        rs[i & 3] = f2_add(rs[i & 3], f2(a, c));
         p1[i] = pack_bf16(a, c);
       }
-      l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       tmem_st_x32(tS, p0);
       tmem_st_x32(tS + 32, p1);
+      float r0, r1;
+      f2_split(f2_add(f2_add(rs[0], rs[1]), f2_add(rs[2], rs[3])), r0, r1);
+      l += r0 + r1;
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(p_full(t));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_done(t), 0));
+    // Every warp of the warpgroup gets here (all waits above are bounded); the
+    // epilogue's named barriers run only if all four warps are on the normal path.
+    ok = named_barrier_and(1 + t, 128, ok);
     if (ok) {
+      // Epilogue: O / l, converted, is written into this tile's Q buffer (no MMA
+      // reads it any more) in the 128-byte-swizzled box layout of the O tensor
+      // map, then stored by TMA as whole 128-byte rows.  fp32 output is twice the
+      // buffer, so it goes in two rounds.
       tc_fence_after_sync();
-      const int q = q0 + t * kBM + row;
-      const bool live = q < args.Sq;
       const float inv_l = 1.0f / l;
-      const long long off = (long long)b * args.o_sb + (long long)q * args.o_ss + (long long)h * args.o_sh;
+      const uint64_t il2 = f2(inv_l, inv_l);
+      const uint32_t stage = base + L::kQ + t * L::kTile;
+      const bool f32 = args.o_f32 != 0;
+      const int W = f32 ? 32 : 64;          // output columns per 128-byte box row
+      const int n_boxes = D / W;            // boxes of 128 rows x 128 bytes per tile
+      constexpr int kPerRound = D / 64;     // boxes that fit in the staging buffer
+      const uint32_t row_addr = stage + row * 128;
+      const uint32_t sw = row & 7;          // 128-byte swizzle: chunk index XOR row % 8
+      const int tile_q0 = q0 + t * kBM;
+      for (int r0 = 0; r0 < n_boxes; r0 += kPerRound) {
+        if (r0 > 0) {  // the previous round's boxes must have been read before reuse
+          if (row == 0) bulk_wait_read_all();
+          named_barrier_sync(1 + t, 128);
+        }
+        for (int c = r0 * W / 32; c < (r0 + kPerRound) * W / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + c * 32, o);
+          const int col0 = c * 32;
+          const uint32_t dst = row_addr + (col0 / W - r0) * L::kBox;
+          const int chunk0 = (col0 % W) / (f32 ? 4 : 8);
+          if (f32) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld_x32(tO + c * 32, o);
-        if (live) {
-          if (args.o_f32) {
-            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(args.o) + off + c * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+            for (int u = 0; u < 8; ++u) {
+              float x0, x1, x2, x3;
+              f2_split(f2_mul(f2(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1])), il2), x0, x1);
+              f2_split(f2_mul(f2(__uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3])), il2), x2, x3);
+              st_shared_v4(dst + (((chunk0 + u) ^ sw) << 4), __float_as_uint(x0), __float_as_uint(x1),
+                           __float_as_uint(x2), __float_as_uint(x3));
+            }
           } else {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.o) + off + c * 32);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
-              dst[i] = v;
+            for (int u = 0; u < 4; ++u) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float x0, x1;
+                f2_split(f2_mul(f2(__uint_as_float(o[8 * u + 2 * e]), __uint_as_float(o[8 * u + 2 * e + 1])), il2),
+                         x0, x1);
+                w[e] = pack_bf16(x0, x1);
+              }
+              st_shared_v4(dst + (((chunk0 + u) ^ sw) << 4), w[0], w[1], w[2], w[3]);
             }
           }
         }
+        fence_proxy_async_smem();
+        named_barrier_sync(1 + t, 128);
+        if (row == 0 && tile_q0 < args.Sq) {
+          for (int bx = 0; bx < kPerRound && r0 + bx < n_boxes; ++bx)
+            tma_store_4d(&tm_o, stage + bx * L::kBox, (r0 + bx) * W, h, tile_q0, b);
+          bulk_commit_group();
+        }
       }
-      if (live) args.lse[((long long)b * args.H + h) * args.Sq + q] = (m + log2f(l)) * 0.69314718055994531f;
+      if (row == 0) bulk_wait_read_all();
+      const int q = tile_q0 + row;
+      if (q < args.Sq) args.lse[((long long)b * args.H + h) * args.Sq + q] = (m + log2f(l)) * 0.69314718055994531f;
     }
   }
 
@@ -375,24 +452,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// bf16 [B, S, H, D] with element strides {b, s, h}, as a 4-D map (d, h, s, b),
-// box 64 x 1 x 128 x 1, 128-byte swizzle; rows past S read as zero.
-bool encode_bshd(CUtensorMap *map, const void *ptr, int B, int S, int H, int D, const int64_t st[3]) {
+// [B, S, H, D] with element strides {b, s, h} (bf16 or fp32) as a 4-D map
+// (d, h, s, b) with a box of 128 bytes x 1 x 128 rows x 1 and 128-byte swizzle;
+// rows past S read as zero and are not written.
+bool encode_bshd(CUtensorMap *map, const void *ptr, int B, int S, int H, int D, const int64_t st[3], bool f32) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)st[2] * es, (cuuint64_t)st[1] * es, (cuuint64_t)st[0] * es};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, 128, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 template <int D>
-cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const AttnArgs &a,
-                         int B, cudaStream_t stream) {
+cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
+                         const AttnArgs &a, int B, cudaStream_t stream) {
   using Lay = Layout<D>;
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
   int dev = 0;
@@ -405,7 +484,7 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     configured[dev] = true;
   }
   dim3 grid((a.Sq + kBM * kNQ - 1) / (kBM * kNQ), a.H, B);
-  attn_fwd_kernel<D><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, a);
+  attn_fwd_kernel<D><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -416,12 +495,12 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
                             void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
                             const char **detail) {
   (void)Skv;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int n_kv = kv_end - kv_begin;
   const char *k0 = static_cast<const char *>(k) + (int64_t)kv_begin * kv_st[1] * 2;
   const char *v0 = static_cast<const char *>(v) + (int64_t)kv_begin * kv_st[1] * 2;
-  if (!encode_bshd(&tq, q, B, Sq, H, D, q_st) || !encode_bshd(&tk, k0, B, n_kv, H, D, kv_st) ||
-      !encode_bshd(&tv, v0, B, n_kv, H, D, kv_st)) {
+  if (!encode_bshd(&tq, q, B, Sq, H, D, q_st, false) || !encode_bshd(&tk, k0, B, n_kv, H, D, kv_st, false) ||
+      !encode_bshd(&tv, v0, B, n_kv, H, D, kv_st, false) || !encode_bshd(&to, o, B, Sq, H, D, o_st, o_f32)) {
     *detail = "cuTensorMapEncodeTiled failed (driver entry point missing or strides/extents unsupported)";
     return cudaErrorInvalidValue;
   }
@@ -436,8 +515,8 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   a.o_sh = o_st[2];
   a.o_f32 = o_f32 ? 1 : 0;
   a.lse = lse;
-  if (D == 64) return launch_typed<64>(tq, tk, tv, a, B, stream);
-  return launch_typed<128>(tq, tk, tv, a, B, stream);
+  if (D == 64) return launch_typed<64>(tq, tk, tv, to, a, B, stream);
+  return launch_typed<128>(tq, tk, tv, to, a, B, stream);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int *value) {
