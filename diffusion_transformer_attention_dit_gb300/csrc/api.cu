@@ -150,10 +150,13 @@ dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const flo
 
 dit_status dit_poll_device_error(struct CUstream_st *stream) {
   g_detail = "";
-  unsigned int v = 0;
-  cudaError_t e = ditattn::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), &v);
+  unsigned int va = 0, vp = 0, vm = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = ditattn::read_and_clear_attn_error(&va);
+  if (e == cudaSuccess) e = ditattn::read_and_clear_prologue_error(&vp);
+  if (e == cudaSuccess) e = ditattn::read_and_clear_merge_error(&vm);
   if (e != cudaSuccess) return from_cuda(e, nullptr);
-  if (v) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (va | vp | vm) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return DIT_OK;
 }
 

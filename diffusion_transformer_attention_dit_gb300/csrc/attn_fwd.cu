@@ -519,9 +519,8 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   return launch_typed<128>(tq, tk, tv, to, a, B, stream);
 }
 
-cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int *value) {
-  cudaError_t e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) return e;
+cudaError_t read_and_clear_attn_error(unsigned int *value) {
+  cudaError_t e;
   unsigned int zero = 0;
   e = cudaMemcpyFromSymbol(value, g_device_error, sizeof(unsigned int));
   if (e != cudaSuccess) return e;

@@ -20,6 +20,7 @@
 #include <math.h>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace ditattn {
 namespace {
@@ -113,6 +114,171 @@ __global__ void __launch_bounds__(kThreads, 4) merge_lse_kernel(const Tin *__res
   if (lane == 0) lse[li] = L;
 }
 
+// ---------------------------------------------------------------- bulk-copy path
+// For D = 128 and C in {2, 4, 8}: a unit is 32 KB / (C * D * size) consecutive rows; each
+// of the C partial slabs of a unit is one 1-D bulk copy (TMA) into a 3-stage
+// shared-memory ring, two persistent CTAs per SM, so ~96 KB per SM is in
+// flight.  The C partial LSEs of each of a thread's rows (rows x C = 8) are held
+// in registers, loaded before the slab wait.
+
+__device__ unsigned int g_merge_error = 0;
+
+constexpr int kStages = 3;
+constexpr int kStageBytes = 32768;
+constexpr int kBulkSmem = kStages * kStageBytes + 8 * kStages;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(&g_merge_error, 1u);
+      return false;
+    }
+  }
+}
+
+template <typename Tin>
+__device__ __forceinline__ void load_vec_smem(uint32_t addr, float (&v)[16 / sizeof(Tin)]);
+template <>
+__device__ __forceinline__ void load_vec_smem<float>(uint32_t addr, float (&v)[4]) {
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
+}
+template <>
+__device__ __forceinline__ void load_vec_smem<__nv_bfloat16>(uint32_t addr, float (&v)[8]) {
+  uint32_t w[4];
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <typename Tin, typename Tout, int D, int C>
+__global__ void __launch_bounds__(kThreads, 2)
+    merge_lse_bulk_kernel(const Tin *o_parts, const float *__restrict__ lse_parts, int H, int Sq, long long n_rows,
+                          long long pso, long long psl, Tout *o, float *lse, long long n_units) {
+  constexpr int N = 16 / sizeof(Tin);  // elements per 16-byte vector
+  constexpr int kLanes = D / N;        // lanes per row
+  constexpr int kRowsPerPass = kThreads / kLanes;
+  constexpr int kUnitRows = kStageBytes / (C * D * (int)sizeof(Tin));
+  constexpr int kRowsPerThread = kUnitRows / kRowsPerPass;
+  constexpr int kSlab = kUnitRows * D * (int)sizeof(Tin);  // bytes of one partial's rows in a unit
+  static_assert(kRowsPerThread >= 1 && kRowsPerThread * kRowsPerPass == kUnitRows, "unit shape");
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t base = smem_u32(smem);
+  const uint32_t bars = base + kStages * kStageBytes;
+  auto full = [&](int st) { return bars + 8u * st; };
+  const int g = threadIdx.x / kLanes, lane = threadIdx.x % kLanes;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(full(st), 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto issue = [&](long long u, int st) {
+    const long long r0 = u * kUnitRows;
+    const long long rows = n_rows - r0 < kUnitRows ? n_rows - r0 : kUnitRows;
+    const uint32_t bytes = static_cast<uint32_t>(rows * D * sizeof(Tin));
+    mbar_arrive_expect_tx(full(st), bytes * C);
+#pragma unroll
+    for (int c = 0; c < C; ++c) bulk_load(base + st * kStageBytes + c * kSlab, o_parts + c * pso + r0 * D, bytes, full(st));
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kStages; ++i) {
+      const long long u = blockIdx.x + (long long)i * gridDim.x;
+      if (u < n_units) {
+        issue(u, i);
+        ++issued;
+      }
+    }
+  int it = 0;
+  for (long long u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+    const int st = it % kStages;
+    const long long r0 = u * kUnitRows;
+    const int rows = static_cast<int>(n_rows - r0 < kUnitRows ? n_rows - r0 : kUnitRows);
+    // the partial LSEs of this thread's rows are fetched before waiting for the slabs
+    long long li[kRowsPerThread];
+    float lv[kRowsPerThread][C];
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      const int row = g + k * kRowsPerPass;
+      const long long gr = r0 + row, bq = gr / H;
+      li[k] = (bq / Sq * H + gr % H) * Sq + bq % Sq;
+#pragma unroll
+      for (int c = 0; c < C; ++c) lv[k][c] = row < rows ? lse_parts[c * psl + li[k]] : -INFINITY;
+    }
+    const bool ok = wait_bounded(full(st), (it / kStages) & 1);
+    if (!__syncthreads_and(ok)) break;
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      const int row = g + k * kRowsPerPass;
+      if (row >= rows) continue;
+      float mx = lv[k][0];
+#pragma unroll
+      for (int c = 1; c < C; ++c) mx = fmaxf(mx, lv[k][c]);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float L = -INFINITY;
+      if (mx != -INFINITY) {
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < C; ++c) sum += expf(lv[k][c] - mx);
+        L = mx + logf(sum);
+        const uint32_t src = base + st * kStageBytes + row * (D * (int)sizeof(Tin)) + lane * 16;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          const float w = expf(lv[k][c] - L);
+          float v[N];
+          load_vec_smem<Tin>(src + c * kSlab, v);
+#pragma unroll
+          for (int i = 0; i < N; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+        }
+      }
+      store_vec<N>(o + (r0 + row) * D + lane * N, acc);
+      if (lane == 0) lse[li[k]] = L;
+    }
+    __syncthreads();  // every thread is done with this stage
+    if (threadIdx.x == 0) {
+      const long long nu = u + (long long)kStages * gridDim.x;
+      if (nu < n_units) {
+        issue(nu, st);
+        ++issued;
+      }
+    }
+  }
+  if (threadIdx.x == 0)
+    for (int j = it; j < issued; ++j) wait_bounded(full(j % kStages), (j / kStages) & 1);
+}
+
+template <typename Tin, typename Tout, int C>
+cudaError_t launch_bulk(const void *o_parts, const float *lse_parts, int B, int H, int Sq, long long pso,
+                        long long psl, void *o, float *lse, cudaStream_t stream) {
+  constexpr int D = 128;
+  static bool configured[64] = {};
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(merge_lse_bulk_kernel<Tin, Tout, D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBulkSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long n_rows = (long long)B * Sq * H;
+  constexpr int kUnitRows = kStageBytes / (C * D * (int)sizeof(Tin));
+  const long long n_units = (n_rows + kUnitRows - 1) / kUnitRows;
+  const long long grid = n_units < 2LL * sms ? n_units : 2LL * sms;
+  merge_lse_bulk_kernel<Tin, Tout, D, C><<<(unsigned)grid, kThreads, kBulkSmem, stream>>>(
+      static_cast<const Tin *>(o_parts), lse_parts, H, Sq, n_rows, pso, psl, static_cast<Tout *>(o), lse, n_units);
+  return cudaGetLastError();
+}
+
 template <typename Tin, typename Tout, int D>
 cudaError_t launch_typed(const void *o_parts, const float *lse_parts, int C, int B, int H, int Sq, long long pso,
                          long long psl, void *o, float *lse, cudaStream_t stream) {
@@ -128,6 +294,10 @@ cudaError_t launch_typed(const void *o_parts, const float *lse_parts, int C, int
 template <typename Tin, typename Tout>
 cudaError_t launch_d(const void *o_parts, const float *lse_parts, int C, int B, int H, int Sq, int D, long long pso,
                      long long psl, void *o, float *lse, cudaStream_t stream) {
+  // bulk-copy path for the common chunk counts at D = 128; everything else row-parallel
+  if (D == 128 && C == 2) return launch_bulk<Tin, Tout, 2>(o_parts, lse_parts, B, H, Sq, pso, psl, o, lse, stream);
+  if (D == 128 && C == 4) return launch_bulk<Tin, Tout, 4>(o_parts, lse_parts, B, H, Sq, pso, psl, o, lse, stream);
+  if (D == 128 && C == 8) return launch_bulk<Tin, Tout, 8>(o_parts, lse_parts, B, H, Sq, pso, psl, o, lse, stream);
   if (D == 64) return launch_typed<Tin, Tout, 64>(o_parts, lse_parts, C, B, H, Sq, pso, psl, o, lse, stream);
   return launch_typed<Tin, Tout, 128>(o_parts, lse_parts, C, B, H, Sq, pso, psl, o, lse, stream);
 }
@@ -135,6 +305,13 @@ cudaError_t launch_d(const void *o_parts, const float *lse_parts, int C, int B, 
 }  // namespace
 
 int merge_max_parts() { return kMaxC; }
+
+cudaError_t read_and_clear_merge_error(unsigned int *value) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_merge_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_merge_error, &zero, sizeof(unsigned int));
+}
 
 bool merge_fits(int C, int H) { return C <= kMaxC && H >= 1; }
 

@@ -25,7 +25,9 @@ cudaError_t launch_merge_lse(const void *o_parts, bool in_f32, const float *lse_
 int merge_max_parts();
 bool merge_fits(int C, int H);
 
-// Read and clear the device word in which bounded waits record that they gave up.
-cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int *value);
+// Read and clear the device words in which each kernel's bounded waits record that they gave up.
+cudaError_t read_and_clear_attn_error(unsigned int *value);
+cudaError_t read_and_clear_prologue_error(unsigned int *value);
+cudaError_t read_and_clear_merge_error(unsigned int *value);
 
 }  // namespace ditattn

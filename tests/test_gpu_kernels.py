@@ -124,7 +124,7 @@ def test_attn_fwd_sharp_softmax_rescale(orc):
 
 # ---------------------------------------------------------------- merge
 
-@pytest.mark.parametrize("C", [1, 2, 3, 8])
+@pytest.mark.parametrize("C", [1, 2, 3, 8, 20])  # 20 parts take the register (non-bulk) path
 @pytest.mark.parametrize("in_dt,out_dt", [("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16"), ("bf16", "f32")])
 def test_merge_parity(orc, C, in_dt, out_dt):
     B, Sq, H, D = 2, 77, 3, 128
