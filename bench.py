@@ -37,6 +37,9 @@ FALLBACK_TFLOPS = 1900.0
 FALLBACK_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480": "f32", "wan720": "bf16"}
+# DRAM bytes per attention launch (read + write) from an ncu capture of the bench step
+# (profiles/launch_list_qwen_image_step.md), valid for the attention source it was taken on.
+ATTN_TRAFFIC = {"source_sha256_prefix": "b02eef41b2adeae0", "qwen_image": (39.0 + 55.8) * 1e6}
 
 
 def peaks():
@@ -193,6 +196,16 @@ def config_of(w, chunks, args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def attn_traffic(name: str):
+    """ncu DRAM bytes per attention launch, or None if the kernel source changed since the capture."""
+    import hashlib
+
+    src = ROOT / "diffusion_transformer_attention_dit_gb300" / "csrc" / "attn_fwd.cu"
+    if hashlib.sha256(src.read_bytes()).hexdigest()[:16] != ATTN_TRAFFIC["source_sha256_prefix"]:
+        return None
+    return ATTN_TRAFFIC.get(name)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -347,7 +360,7 @@ def run_ours(args):
             "config": config_of(w, chunks, args),
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved, "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": achieved / peak_tf, "peak_source": src,
-                         "traffic": args.traffic},
+                         "traffic": args.traffic if args.traffic is not None else attn_traffic(w.name)},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(),
