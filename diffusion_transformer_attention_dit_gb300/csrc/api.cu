@@ -160,4 +160,9 @@ dit_status dit_poll_device_error(struct CUstream_st *stream) {
   return DIT_OK;
 }
 
+dit_status dit_selftest_wait_timeout(struct CUstream_st *stream) {
+  g_detail = "";
+  return from_cuda(ditattn::launch_wait_timeout_selftest(reinterpret_cast<cudaStream_t>(stream)), nullptr);
+}
+
 }  // extern "C"

@@ -55,6 +55,7 @@ constexpr int kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold on the running max (base-2 units)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitLimitIters = 1u << 26;
 constexpr unsigned int kErrWaitTimeout = 1u;
 
 template <int D>
@@ -87,7 +88,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    // two bounds: elapsed time, and an iteration count that ends the wait even if
+    // the global timer were not advancing
+    if ((i & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || i > kWaitLimitIters)) {
       atomicOr(&g_device_error, kErrWaitTimeout);
       return false;
     }
@@ -438,6 +441,17 @@ const uint64_t nm2 = f2(-m, -m);
   }
 }
 
+// One thread waits, with the same bounded wait as the attention kernel, on an
+// mbarrier that nothing ever arrives at: the wait must give up, record the
+// timeout in the error word and let the kernel return.
+__global__ void wait_timeout_selftest_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t addr = smem_u32(&bar);
+  mbar_init(addr, 1);
+  mbar_fence_init();
+  wait_bounded(addr, 0);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -517,6 +531,11 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   a.lse = lse;
   if (D == 64) return launch_typed<64>(tq, tk, tv, to, a, B, stream);
   return launch_typed<128>(tq, tk, tv, to, a, B, stream);
+}
+
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 1, 0, stream>>>();
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_attn_error(unsigned int *value) {

@@ -46,6 +46,21 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&v)[8]) 
   }
 }
 
+// Hardware base-2 exponential / logarithm (ex2.approx / lg2.approx, ~2 ulp): the
+// merge weights exp(L_c - L) and L = m + ln(sum) are formed in base 2.
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -91,15 +106,15 @@ __global__ void __launch_bounds__(kThreads, 4) merge_lse_kernel(const Tin *__res
     return;
   }
   float sum = 0.f;
-  for (int c = 0; c < C; ++c) sum += expf(lse_parts[c * psl + li] - mx);
-  const float L = mx + logf(sum);
+  for (int c = 0; c < C; ++c) sum += fast_ex2((lse_parts[c * psl + li] - mx) * kLog2e);
+  const float L = mx + fast_lg2(sum) * kLn2;
   for (int c0 = 0; c0 < C; c0 += kGroup) {
     float v[kGroup][N], w[kGroup];
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
       if (c0 + u < C) {
         load_vec(o_parts + (c0 + u) * pso + off, v[u]);
-        w[u] = expf(lse_parts[(c0 + u) * psl + li] - L);
+        w[u] = fast_ex2((lse_parts[(c0 + u) * psl + li] - L) * kLog2e);
       }
     }
 #pragma unroll
@@ -127,13 +142,16 @@ constexpr int kStages = 3;
 constexpr int kStageBytes = 32768;
 constexpr int kBulkSmem = kStages * kStageBytes + 8 * kStages;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitLimitIters = 1u << 26;
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    // two bounds: elapsed time, and an iteration count that ends the wait even if
+    // the global timer were not advancing
+    if ((i & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || i > kWaitLimitIters)) {
       atomicOr(&g_merge_error, 1u);
       return false;
     }
@@ -226,12 +244,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (mx != -INFINITY) {
         float sum = 0.f;
 #pragma unroll
-        for (int c = 0; c < C; ++c) sum += expf(lv[k][c] - mx);
-        L = mx + logf(sum);
+        for (int c = 0; c < C; ++c) sum += fast_ex2((lv[k][c] - mx) * kLog2e);
+        L = mx + fast_lg2(sum) * kLn2;
         const uint32_t src = base + st * kStageBytes + row * (D * (int)sizeof(Tin)) + lane * 16;
 #pragma unroll
         for (int c = 0; c < C; ++c) {
-          const float w = expf(lv[k][c] - L);
+          const float w = fast_ex2((lv[k][c] - L) * kLog2e);
           float v[N];
           load_vec_smem<Tin>(src + c * kSlab, v);
 #pragma unroll

@@ -25,6 +25,9 @@ cudaError_t launch_merge_lse(const void *o_parts, bool in_f32, const float *lse_
 int merge_max_parts();
 bool merge_fits(int C, int H);
 
+// One-thread kernel whose bounded wait on a never-completed mbarrier must give up.
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
+
 // Read and clear the device words in which each kernel's bounded waits record that they gave up.
 cudaError_t read_and_clear_attn_error(unsigned int *value);
 cudaError_t read_and_clear_prologue_error(unsigned int *value);

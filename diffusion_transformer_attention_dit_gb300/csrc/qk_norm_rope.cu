@@ -32,13 +32,16 @@ constexpr int kStages = 3;
 constexpr int kUnitBytes = 16384;  // bytes of q (and of k) per unit
 constexpr int kSmem = kStages * 2 * kUnitBytes + 8 * kStages;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitLimitIters = 1u << 26;
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    // two bounds: elapsed time, and an iteration count that ends the wait even if
+    // the global timer were not advancing
+    if ((i & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || i > kWaitLimitIters)) {
       atomicOr(&g_prologue_error, 1u);
       return false;
     }

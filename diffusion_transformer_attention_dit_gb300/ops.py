@@ -19,7 +19,7 @@ LIBRARY = Path(__file__).resolve().parent / "libditattn.so"
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
 DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
-            "dit_status_string", "dit_last_error_detail")
+            "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout")
 
 _lib = None
 
@@ -47,7 +47,9 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_attn_merge_lse.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_int64, ctypes.c_int64, vp,
                                        i32, vp, vp]
     lib.dit_poll_device_error.argtypes = [vp]
-    for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error"):
+    lib.dit_selftest_wait_timeout.argtypes = [vp]
+    for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
+                 "dit_selftest_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -162,6 +164,11 @@ def attn_merge_lse(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=Non
 def poll_device_error(stream=None):
     """Synchronise the stream and raise DitError if a bounded device-side wait gave up since the last poll."""
     _check(load_library().dit_poll_device_error(_stream(stream)))
+
+
+def selftest_wait_timeout(stream=None):
+    """Run the bounded-wait self-test kernel; a following poll_device_error() must raise DIT_ERR_TIMEOUT."""
+    _check(load_library().dit_selftest_wait_timeout(_stream(stream)))
 
 
 def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1, scale: float | None = None,

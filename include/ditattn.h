@@ -15,9 +15,9 @@
  *     BNSD.  LSE is fp32 [B, H, Sq], contiguous.
  *   - bf16 means IEEE bfloat16 (stored as 16-bit words); fp32 is IEEE binary32.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
- *     default stream) and allocates no device memory.  The library owns one
- *     static device word that records a device-side wait that gave up (see
- *     dit_poll_device_error).
+ *     default stream) and allocates no device memory.  The library owns a few
+ *     static device words (one per kernel family) that record a device-side
+ *     wait that gave up (see dit_poll_device_error).
  *   - Argument errors return DIT_ERR_INVALID_ARG / DIT_ERR_UNSUPPORTED before
  *     anything is launched.  A launch failure returns DIT_ERR_CUDA.  Work of
  *     size zero (B, H or a sequence length 0) returns DIT_OK and launches
@@ -151,6 +151,17 @@ dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const flo
  * synchronisation itself failed.
  */
 dit_status dit_poll_device_error(struct CUstream_st *stream);
+
+/*
+ * dit_selftest_wait_timeout -- failure-detection self-test.  Launches one thread
+ * that waits, with the same bounded wait every kernel here uses, on a device
+ * barrier that nothing ever completes; the wait gives up after about 2 s and
+ * records the timeout.  A following dit_poll_device_error must then return
+ * DIT_ERR_TIMEOUT, with the CUDA context still usable.  Not part of the
+ * attention path (the pages have no counterpart); it exercises the error
+ * route that a stalled pipeline would take.
+ */
+dit_status dit_selftest_wait_timeout(struct CUstream_st *stream);
 
 /* dit_status_string -- static, human-readable name of a status code (never NULL). */
 const char *dit_status_string(dit_status s);

@@ -202,3 +202,20 @@ def test_full_hot_path_tiny(orc):
                                    out_dtype=out_dt)
         check_o(host_f64(o), ro, f32=out_dt == torch.float32, what="tiny hot path", vmax=vmax(inp.v))
         check_lse(host_f64(lse), rl, what="tiny hot path")
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """A wait on a barrier nothing completes gives up (~2 s) and is reported; later launches still work."""
+    import time
+
+    ops.poll_device_error()  # clear
+    t0 = time.time()
+    ops.selftest_wait_timeout()
+    with pytest.raises(ops.DitError) as e:
+        ops.poll_device_error()
+    assert e.value.status == ops.DIT_ERR_TIMEOUT
+    assert time.time() - t0 < 30
+    ops.poll_device_error()  # cleared by the previous poll
+    q, k, v, *_ = inputs.small_case(1, 128, 1, 64, seed=5)
+    o, _ = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v))
+    assert torch.isfinite(o.float()).all()
