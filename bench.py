@@ -206,6 +206,22 @@ def attn_traffic(name: str):
     return ATTN_TRAFFIC.get(name)
 
 
+def aggregate(t_local: float, flops_per_step: float, steps: int, world: int, device=None):
+    """Replica timing across ranks: max of the per-rank timed seconds, and whole-job TFLOP/s.
+
+    Each rank runs its own full copy of the workload (no data-path collective);
+    the process group only carries this max-reduction.
+    """
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([t_local], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t_max = float(t.item())
+    return t_max, flops_per_step * steps * world / t_max / 1e12
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -306,12 +322,8 @@ def run_ours(args):
     ops.poll_device_error()
     t_steps = sum(a.elapsed_time(b) for a, b in step_ms) / 1e3
     t_attn = sum(a.elapsed_time(b) for a, b in attn_ms) / 1e3
-    t = torch.tensor([t_steps], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    t_max = t.item()
     flops_step = w.attention_flops()
-    value = flops_step * args.steps * world / t_max / 1e12
+    t_max, value = aggregate(t_steps, flops_step, args.steps, world, dev)
 
     # end to end through the public API: pinned host inputs in, O and LSE back to pinned host memory
     pin = {n: torch.from_numpy(np.ascontiguousarray(host[n]).view(np.int16)).pin_memory() for n in host}
@@ -345,10 +357,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_t += e0.elapsed_time(e1) / 1e3
-    et = torch.tensor([e2e_t], device=dev)
-    if world > 1:
-        dist.all_reduce(et, op=dist.ReduceOp.MAX)
-    e2e_value = flops_step * args.steps * world / et.item() / 1e12
+    _, e2e_value = aggregate(e2e_t, flops_step, args.steps, world, dev)
 
     if rank == 0:
         peak_tf, peak_gbs, src = peaks()
