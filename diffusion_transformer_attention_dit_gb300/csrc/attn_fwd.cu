@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (i >= valid) s[i] = -INFINITY;
       }
-        // row max: 3-input max over 4 independent chains, then a tree
+      // row max: 3-input max over 4 independent chains, then a tree
       float mp[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
       for (int i = 4; i < kBN - 4; i += 8)
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-const uint64_t nm2 = f2(-m, -m);
+      const uint64_t nm2 = f2(-m, -m);
       uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};  // packed row-sum partials (0.0f bit patterns)
       uint32_t p0[32], p1[32];
 #pragma unroll
