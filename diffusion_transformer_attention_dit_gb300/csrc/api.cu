@@ -77,10 +77,14 @@ dit_status dit_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_o
                    nullptr);
 }
 
-dit_status dit_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
-                        const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
-                        int kv_end, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
-                        struct CUstream_st *stream) {
+}  // extern "C"
+
+namespace {
+
+dit_status attn_common(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                       const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin, int kv_end,
+                       bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                       struct CUstream_st *stream) {
   g_detail = "";
   if (B < 0 || H < 0 || Sq < 0 || Skv < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
   if (D != 64 && D != 128) return fail(DIT_ERR_UNSUPPORTED, "head dim must be 64 or 128");
@@ -111,9 +115,29 @@ dit_status dit_attn_fwd(const void *q, const void *k, const void *v, int B, int 
     return fail(DIT_ERR_INVALID_ARG, "outputs overlap inputs or each other");
   const char *detail = nullptr;
   cudaError_t e = ditattn::launch_attn_fwd(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end,
-                                           o, o_dtype == DIT_F32, o_strides, lse,
+                                           causal, o, o_dtype == DIT_F32, o_strides, lse,
                                            reinterpret_cast<cudaStream_t>(stream), &detail);
   return from_cuda(e, detail);
+}
+
+}  // namespace
+
+extern "C" {
+
+dit_status dit_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                        const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
+                        int kv_end, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                        struct CUstream_st *stream) {
+  return attn_common(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end, false, o, o_dtype,
+                     o_strides, lse, stream);
+}
+
+dit_status dit_attn_fwd_causal(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                               const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
+                               int kv_end, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                               struct CUstream_st *stream) {
+  return attn_common(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end, true, o, o_dtype,
+                     o_strides, lse, stream);
 }
 
 dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const float *lse_parts, int C, int B, int H,
@@ -158,6 +182,43 @@ dit_status dit_poll_device_error(struct CUstream_st *stream) {
   if (e != cudaSuccess) return from_cuda(e, nullptr);
   if (va | vp | vm) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return DIT_OK;
+}
+
+dit_status dit_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y, int B, int L,
+                                   int C, float eps, struct CUstream_st *stream) {
+  g_detail = "";
+  if (B < 0 || L < 0 || C < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if (C % 8 || C > ditattn::row_norm_max_channels())
+    return fail(DIT_ERR_UNSUPPORTED, "C must be a multiple of 8 and at most 8192");
+  if (!(eps >= 0.f) || isinf(eps)) return fail(DIT_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if ((int64_t)B * L * C == 0) return DIT_OK;
+  if (!x || !y) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(scale, 4) || !aligned(shift, 4))
+    return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const uintptr_t n = (uintptr_t)B * L * C * 2;
+  const Range rx = {reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + n};
+  const Range ry = {reinterpret_cast<uintptr_t>(y), reinterpret_cast<uintptr_t>(y) + n};
+  if (x != y && overlap(rx, ry)) return fail(DIT_ERR_INVALID_ARG, "y overlaps x (only exact in-place is allowed)");
+  return from_cuda(ditattn::launch_layer_norm_modulate(x, scale, shift, y, B, L, C, eps,
+                                                       reinterpret_cast<cudaStream_t>(stream)),
+                   nullptr);
+}
+
+dit_status dit_rms_norm(const void *x, const float *w, void *y, int64_t rows, int C, float eps,
+                        struct CUstream_st *stream) {
+  g_detail = "";
+  if (rows < 0 || C < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if (C % 8 || C > ditattn::row_norm_max_channels())
+    return fail(DIT_ERR_UNSUPPORTED, "C must be a multiple of 8 and at most 8192");
+  if (!(eps >= 0.f) || isinf(eps)) return fail(DIT_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (rows * C == 0) return DIT_OK;
+  if (!x || !y || !w) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 4)) return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const uintptr_t n = (uintptr_t)rows * C * 2;
+  const Range rx = {reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + n};
+  const Range ry = {reinterpret_cast<uintptr_t>(y), reinterpret_cast<uintptr_t>(y) + n};
+  if (x != y && overlap(rx, ry)) return fail(DIT_ERR_INVALID_ARG, "y overlaps x (only exact in-place is allowed)");
+  return from_cuda(ditattn::launch_rms_norm(x, w, y, rows, C, eps, reinterpret_cast<cudaStream_t>(stream)), nullptr);
 }
 
 dit_status dit_selftest_wait_timeout(struct CUstream_st *stream) {

@@ -75,6 +75,7 @@ struct Layout {
 
 struct AttnArgs {
   int H, Sq, n_kv;
+  int kv_begin;  // absolute index of the first key of the range
   float scale_log2;
   void *o;
   long long o_sb, o_ss, o_sh;
@@ -139,7 +140,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int D>
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -153,7 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
   const int q0 = blockIdx.x * (kBM * kNQ);
-  const int nblk = (args.n_kv + kBN - 1) / kBN;
+  // key blocks this CTA visits: all of the range, or (causal) those up to its last query row
+  int nblk = (args.n_kv + kBN - 1) / kBN;
+  if (kCausal) {
+    const int q_last = min(q0 + kBM * kNQ, args.Sq) - 1;
+    const int reach = q_last - args.kv_begin + 1;  // keys of the range visible to the last row
+    nblk = max(1, min(nblk, (reach + kBN - 1) / kBN));
+  }
 
   const uint32_t bars = base + L::kBar;
   const uint32_t q_full = bars;
@@ -300,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s[128];
 #pragma unroll
       for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sr[i]);
-      const int valid = args.n_kv - j * kBN;
+      // columns past the range end, and (causal) keys after this row, are masked
+      int valid = args.n_kv - j * kBN;
+      if (kCausal) valid = min(valid, q0 + t * kBM + row - args.kv_begin - j * kBN + 1);
       if (valid < kBN) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
@@ -321,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The previous PV product of this tile is complete: S_t for block j was
         // issued after it and its commit covers every earlier MMA.
         const float m_new = fmaxf(m, mx);
-        const float alpha = ex2(m - m_new);
+        // (causal) rows that have seen no key yet keep m = -inf and O = 0
+        const float alpha = (kCausal && m_new == -INFINITY) ? 1.f : ex2(m - m_new);
         m = m_new;
         l *= alpha;
 #pragma unroll
@@ -334,7 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
-      const uint64_t nm2 = f2(-m, -m);
+      // (causal) a row that has seen no key yet keeps m = -inf: its weights are all zero
+      const float m_use = (kCausal && m == -INFINITY) ? 0.f : m;
+      const uint64_t nm2 = f2(-m_use, -m_use);
       uint64_t rs[4] = {0ull, 0ull, 0ull, 0ull};  // packed row-sum partials (0.0f bit patterns)
       uint32_t p0[32], p1[32];
 #pragma unroll
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // map, then stored by TMA as whole 128-byte rows.  fp32 output is twice the
       // buffer, so it goes in two rounds.
       tc_fence_after_sync();
-      const float inv_l = 1.0f / l;
+      const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row with no visible key outputs zeros
       const uint64_t il2 = f2(inv_l, inv_l);
       const uint32_t stage = base + L::kQ + t * L::kTile;
       const bool f32 = args.o_f32 != 0;
@@ -429,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (row == 0) bulk_wait_read_all();
       const int q = tile_q0 + row;
-      if (q < args.Sq) args.lse[((long long)b * args.H + h) * args.Sq + q] = (m + log2f(l)) * 0.69314718055994531f;
+      if (q < args.Sq)
+        args.lse[((long long)b * args.H + h) * args.Sq + q] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -483,7 +496,7 @@ bool encode_bshd(CUtensorMap *map, const void *ptr, int B, int S, int H, int D, 
   return r == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kCausal>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
                          const AttnArgs &a, int B, cudaStream_t stream) {
   using Lay = Layout<D>;
@@ -493,12 +506,12 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   dim3 grid((a.Sq + kBM * kNQ - 1) / (kBM * kNQ), a.H, B);
-  attn_fwd_kernel<D><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, to, a);
+  attn_fwd_kernel<D, kCausal><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -506,7 +519,7 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                             const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
-                            void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
+                            bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
                             const char **detail) {
   (void)Skv;
   CUtensorMap tq, tk, tv, to;
@@ -522,6 +535,7 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   a.H = H;
   a.Sq = Sq;
   a.n_kv = n_kv;
+  a.kv_begin = kv_begin;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.o = o;
   a.o_sb = o_st[0];
@@ -529,8 +543,11 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   a.o_sh = o_st[2];
   a.o_f32 = o_f32 ? 1 : 0;
   a.lse = lse;
-  if (D == 64) return launch_typed<64>(tq, tk, tv, to, a, B, stream);
-  return launch_typed<128>(tq, tk, tv, to, a, B, stream);
+  if (causal)
+    return D == 64 ? launch_typed<64, true>(tq, tk, tv, to, a, B, stream)
+                   : launch_typed<128, true>(tq, tk, tv, to, a, B, stream);
+  return D == 64 ? launch_typed<64, false>(tq, tk, tv, to, a, B, stream)
+                 : launch_typed<128, false>(tq, tk, tv, to, a, B, stream);
 }
 
 cudaError_t launch_wait_timeout_selftest(cudaStream_t stream) {

@@ -7,10 +7,11 @@
 
 namespace ditattn {
 
-// Attention forward over keys [kv_begin, kv_end).  Strides in elements {b, s, h}.
+// Attention forward over keys [kv_begin, kv_end) (causal: query i sees keys j <= i).
+// Strides in elements {b, s, h}.
 cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                             const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
-                            void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
+                            bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
                             const char **detail);
 
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,
@@ -20,6 +21,13 @@ cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void 
 cudaError_t launch_merge_lse(const void *o_parts, bool in_f32, const float *lse_parts, int C, int B, int H, int Sq,
                              int D, int64_t part_stride_o, int64_t part_stride_lse, void *o, bool out_f32,
                              float *lse, cudaStream_t stream);
+
+// Row normalisations (LayerNorm + adaLN modulation; RMSNorm over C).  C % 8 == 0, C <= row_norm_max_channels().
+int row_norm_max_channels();
+cudaError_t launch_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y, int B, int L,
+                                       int C, float eps, cudaStream_t stream);
+cudaError_t launch_rms_norm(const void *x, const float *w, void *y, long long rows, int C, float eps,
+                            cudaStream_t stream);
 
 // Largest C the merge kernel accepts, and whether C * H weights fit its shared-memory budget.
 int merge_max_parts();

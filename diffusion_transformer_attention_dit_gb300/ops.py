@@ -19,7 +19,8 @@ LIBRARY = Path(__file__).resolve().parent / "libditattn.so"
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
 DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
-            "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout")
+            "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
+            "dit_layer_norm_modulate", "dit_rms_norm")
 
 _lib = None
 
@@ -44,12 +45,15 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_qk_norm_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp]
     lib.dit_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i64p, i64p, f32, i32, i32, vp, i32, i64p,
                                  vp, vp]
+    lib.dit_attn_fwd_causal.argtypes = lib.dit_attn_fwd.argtypes
     lib.dit_attn_merge_lse.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_int64, ctypes.c_int64, vp,
                                        i32, vp, vp]
+    lib.dit_layer_norm_modulate.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, vp]
+    lib.dit_rms_norm.argtypes = [vp, vp, vp, ctypes.c_int64, i32, f32, vp]
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
-    for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
-                 "dit_selftest_wait_timeout"):
+    for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
+                 "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -114,8 +118,10 @@ def qk_norm_rope(q, k, wq, wk, cos, sin, eps: float = 1e-6, q_out=None, k_out=No
 
 
 def attn_fwd(q, k, v, scale: float | None = None, kv_begin: int = 0, kv_end: int | None = None, o=None, lse=None,
-             o_dtype=torch.bfloat16, stream=None):
-    """Flash attention forward over keys [kv_begin, kv_end).  Returns (o [B, Sq, H, D], lse fp32 [B, H, Sq])."""
+             o_dtype=torch.bfloat16, stream=None, causal: bool = False):
+    """Flash attention forward over keys [kv_begin, kv_end).  Returns (o [B, Sq, H, D], lse fp32 [B, H, Sq]).
+
+    causal=True masks keys after each query (query i sees keys j <= i)."""
     lib = load_library()
     _cuda(q, k, v)
     B, Sq, H, D = q.shape
@@ -134,7 +140,8 @@ def attn_fwd(q, k, v, scale: float | None = None, kv_begin: int = 0, kv_end: int
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, H, Sq):
         raise ValueError("lse must be contiguous fp32 [B, H, Sq]")
-    _check(lib.dit_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq, Skv, D, _bshd_strides(q),
+    fn = lib.dit_attn_fwd_causal if causal else lib.dit_attn_fwd
+    _check(fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq, Skv, D, _bshd_strides(q),
                             _bshd_strides(k), float(scale), int(kv_begin), int(kv_end), o.data_ptr(),
                             _dtype_code(o.dtype), _bshd_strides(o), lse.data_ptr(), _stream(stream)))
     return o, lse
@@ -159,6 +166,37 @@ def attn_merge_lse(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=Non
                                   D, o_parts.stride(0), lse_parts.stride(0), o.data_ptr(), _dtype_code(o.dtype),
                                   lse.data_ptr(), _stream(stream)))
     return o, lse
+
+
+def layer_norm_modulate(x, scale=None, shift=None, eps: float = 1e-6, y=None, stream=None):
+    """LayerNorm over C with adaLN modulation: x bf16 [B, L, C]; scale, shift fp32 [B, C] (or None)."""
+    lib = load_library()
+    _cuda(x)
+    B, L, C = x.shape
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("x must be contiguous bf16 [B, L, C]")
+    for t in (scale, shift):
+        if t is not None and (not t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != (B, C)
+                              or not t.is_contiguous()):
+            raise ValueError("scale / shift must be contiguous fp32 [B, C] on the GPU")
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.dit_layer_norm_modulate(x.data_ptr(), 0 if scale is None else scale.data_ptr(),
+                                       0 if shift is None else shift.data_ptr(), y.data_ptr(), B, L, C, float(eps),
+                                       _stream(stream)))
+    return y
+
+
+def rms_norm(x, w, eps: float = 1e-6, y=None, stream=None):
+    """RMSNorm over the last dim C of a contiguous bf16 tensor with fp32 weight [C]."""
+    lib = load_library()
+    _cuda(x, w)
+    C = x.shape[-1]
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or w.dtype != torch.float32 or w.numel() != C:
+        raise ValueError("x must be contiguous bf16 [..., C] and w fp32 [C]")
+    y = torch.empty_like(x) if y is None else y
+    _check(lib.dit_rms_norm(x.data_ptr(), w.data_ptr(), y.data_ptr(), x.numel() // C, C, float(eps),
+                            _stream(stream)))
+    return y
 
 
 def poll_device_error(stream=None):

@@ -7,6 +7,7 @@
  *   dit_attn_fwd        non-causal flash attention forward -> O and fp32 LSE,
  *                       over all keys or over one key chunk [kv_begin, kv_end)
  *   dit_attn_merge_lse  blockwise log-sum-exp merge of per-chunk (O_c, LSE_c)
+ *   dit_attn_fwd_causal the attention with a causal mask (the pages' VLM path)
  *
  * Conventions shared by every entry point
  *   - Tensors are device pointers owned by the caller.  Activations are
@@ -115,6 +116,27 @@ dit_status dit_attn_fwd(const void *q, const void *k, const void *v,
                         struct CUstream_st *stream);
 
 /*
+ * dit_attn_fwd_causal -- the same as dit_attn_fwd with a causal mask: query i
+ * sees key j only if j <= i (absolute indices, top-left aligned, so a key
+ * chunk [kv_begin, kv_end) masks by kv_begin + local index).  Rows that see no
+ * key of the range get O = 0 and LSE = -inf, which dit_attn_merge_lse treats as
+ * an empty block.
+ *
+ * Defined by: "Cosmos Ascend NPU multi-card parallel optimisation notes",
+ * section 3.1 (the Qwen2.5-VL reasoner's attention: npu_fusion_attention with
+ * sparse_mode=2, or scaled_dot_product_attention with is_causal=True) and "NPU
+ * Wan2.2-I2V model inference optimisation practice", section "NPU
+ * npu_fused_infer_attention_score operator adaptation" (next_tokens=0 when
+ * causal).  Arguments, layouts and errors as for dit_attn_fwd.
+ */
+dit_status dit_attn_fwd_causal(const void *q, const void *k, const void *v,
+                               int B, int H, int Sq, int Skv, int D,
+                               const int64_t q_strides[3], const int64_t kv_strides[3],
+                               float scale, int kv_begin, int kv_end,
+                               void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                               struct CUstream_st *stream);
+
+/*
  * dit_attn_merge_lse -- merge C partial attention results over disjoint key blocks.
  *
  * Defined by: "feat: support Ascend NPU backend (torch_npu) for Qwen-Image
@@ -143,6 +165,41 @@ dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const flo
                               int C, int B, int H, int Sq, int D,
                               int64_t part_stride_o, int64_t part_stride_lse,
                               void *o, dit_dtype out_dtype, float *lse, struct CUstream_st *stream);
+
+/*
+ * dit_layer_norm_modulate -- LayerNorm over C with adaLN modulation, per token.
+ *
+ * Defined by: "NPU Wan2.2-I2V model inference optimisation practice", section
+ * "NPU layer_norm_eval operator adaptation" (WanLayerNorm, eps 1e-6, no affine
+ * parameters; FusedLayerNormModulate folds the modulation into one layer-norm
+ * call with weight 1 + scale and bias shift).
+ *
+ * For every row x of C channels of sample b:
+ *   y = (x - mean(x)) / sqrt(var(x) + eps) * (1 + scale[b]) + shift[b]
+ * with the biased variance; fp32 arithmetic, one bf16 rounding.
+ *
+ *   x, y           bf16 [B, L, C], contiguous, 16-byte aligned; y may equal x
+ *   scale, shift   fp32 [B, C] (one modulation vector per sample), or NULL for 0
+ *   C              a multiple of 8, at most 8192 (else DIT_ERR_UNSUPPORTED)
+ */
+dit_status dit_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y,
+                                   int B, int L, int C, float eps, struct CUstream_st *stream);
+
+/*
+ * dit_rms_norm -- RMSNorm over all C channels of each row: y = x * w / sqrt(mean(x^2) + eps).
+ *
+ * Defined by: "NPU Wan2.2-I2V model inference optimisation practice", section
+ * "NPU rms_norm operator adaptation" (WanRMSNorm on x of shape [B, L, C]) and
+ * "Cosmos Ascend NPU multi-card parallel optimisation notes", section 3.2.
+ * The QK prologue (dit_qk_norm_rope) normalises each head over D; this is the
+ * whole-token variant.
+ *
+ *   x, y   bf16 [rows, C], contiguous, 16-byte aligned; y may equal x
+ *   w      fp32 [C]
+ *   C      a multiple of 8, at most 8192
+ */
+dit_status dit_rms_norm(const void *x, const float *w, void *y, int64_t rows, int C, float eps,
+                        struct CUstream_st *stream);
 
 /*
  * dit_poll_device_error -- synchronise `stream`, then read and clear the

@@ -52,15 +52,20 @@ class Oracle:
         lib = ctypes.CDLL(str(self.path))
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_rms_norm.argtypes = [_D, _D, _I64, _I64, ctypes.c_double, _D]
+        lib.oracle_layer_norm_modulate.argtypes = [_D, _D, _D, _I64, _I64, _I64, ctypes.c_double, _D]
+        lib.oracle_layer_norm_modulate.restype = None
         lib.oracle_rope_interleaved.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _D]
         lib.oracle_qk_norm_rope.argtypes = [_D, _D, _D, _D, _I64, _I64, _I64, _I64, ctypes.c_double, _D]
         lib.oracle_attention.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
                                          _I64, _I64, ctypes.POINTER(ctypes.c_int64), _I64, _D, _D]
+        lib.oracle_attention_masked.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
+                                                _I64, _I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int64), _I64, _D,
+                                                _D]
         lib.oracle_attention_probs.argtypes = [_D, _D, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
                                                _I64, _I64, _D]
         lib.oracle_merge_lse.argtypes = [_D, _D, _I64, _I64, _I64, _I64, _I64, _D, _D]
         for name in ("oracle_rms_norm", "oracle_rope_interleaved", "oracle_qk_norm_rope",
-                     "oracle_attention", "oracle_attention_probs", "oracle_merge_lse"):
+                     "oracle_attention", "oracle_attention_masked", "oracle_attention_probs", "oracle_merge_lse"):
             getattr(lib, name).restype = None
         self.lib = lib
 
@@ -73,6 +78,17 @@ class Oracle:
         D = x.shape[-1]
         y = np.empty_like(x)
         self.lib.oracle_rms_norm(_ptr(x), _ptr(w), x.size // D, D, eps, _ptr(y))
+        return y
+
+    def layer_norm_modulate(self, x, scale, shift, eps: float) -> np.ndarray:
+        """x [B, L, C]; scale, shift [B, C] or None -> LN(x) * (1 + scale) + shift."""
+        x = _f64(x)
+        B, L, C = x.shape
+        sc = None if scale is None else _f64(scale)
+        sh = None if shift is None else _f64(shift)
+        y = np.empty_like(x)
+        self.lib.oracle_layer_norm_modulate(_ptr(x), None if sc is None else _ptr(sc), None if sh is None else _ptr(sh),
+                                            B, L, C, eps, _ptr(y))
         return y
 
     def rope_interleaved(self, x, cos, sin) -> np.ndarray:
@@ -95,8 +111,11 @@ class Oracle:
         self.lib.oracle_qk_norm_rope(_ptr(x), _ptr(w), _ptr(cos), _ptr(sin), B, S, H, D, eps, _ptr(y))
         return y
 
-    def attention(self, q, k, v, scale: float, kv_begin: int = 0, kv_end: int | None = None, rows=None):
-        """q [B, Sq, H, D], k/v [B, Skv, H, D] -> (o [B, nrows, H, D], lse [B, H, nrows])."""
+    def attention(self, q, k, v, scale: float, kv_begin: int = 0, kv_end: int | None = None, rows=None,
+                  causal: bool = False):
+        """q [B, Sq, H, D], k/v [B, Skv, H, D] -> (o [B, nrows, H, D], lse [B, H, nrows]).
+
+        causal: query i sees only keys j <= i (top-left aligned)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
         B, Sq, H, D = q.shape
         Skv = k.shape[1]
@@ -108,8 +127,8 @@ class Oracle:
             nrows, rows_p = rows.size, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
         o = np.empty((B, nrows, H, D))
         lse = np.empty((B, H, nrows))
-        self.lib.oracle_attention(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Skv, D, scale, kv_begin, kv_end,
-                                  rows_p, nrows, _ptr(o), _ptr(lse))
+        self.lib.oracle_attention_masked(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Skv, D, scale, kv_begin, kv_end,
+                                         int(bool(causal)), rows_p, nrows, _ptr(o), _ptr(lse))
         return o, lse
 
     def attention_probs(self, q, k, scale: float, kv_begin: int = 0, kv_end: int | None = None) -> np.ndarray:

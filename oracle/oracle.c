@@ -23,7 +23,11 @@
  *               page section 3.3 (apply_rotary_pos_emb via cos/sin of freqs).
  *   Attention-- same Wan2.2 page, section "NPU npu_fused_infer_attention_score
  *               operator adaptation": non-causal multi-head softmax(scale*QK^T)V
- *               whose second output is the log-sum-exp.
+ *               whose second output is the log-sum-exp.  Causal masking (query
+ *               i sees keys j <= i) is the VLM attention of the Cosmos page,
+ *               section 3.1 (npu_fusion_attention with sparse_mode=2 /
+ *               scaled_dot_product_attention with is_causal=True), and the
+ *               Wan2.2 page's next_tokens=0 for the causal case.
  *   LSE merge-- "feat: support Ascend NPU backend (torch_npu) for Qwen-Image
  *               pipelines - #274", item 2 (models/basic/attention.py: the ring
  *               path combines per-block outputs with update_out_and_lse); the
@@ -60,6 +64,36 @@ void oracle_rms_norm(const double *x, const double *w, int64_t rows, int64_t D, 
         double ms = ss / (double)D;
         double inv = 1.0 / sqrt(ms + eps);
         for (int64_t d = 0; d < D; ++d) yr[d] = xr[d] * inv * w[d];
+    }
+}
+
+/*
+ * LayerNorm with adaLN modulation over the last dimension C of x [B, L, C]:
+ *   mu = mean_c x_c,  var = mean_c (x_c - mu)^2        (biased variance)
+ *   y_c = (x_c - mu) / sqrt(var + eps) * (1 + scale[b, c]) + shift[b, c]
+ * scale / shift are [B, C] (one modulation per sample); either may be NULL (0).
+ * "NPU Wan2.2-I2V model inference optimisation practice", section
+ * "NPU layer_norm_eval operator adaptation" (WanLayerNorm without affine
+ * parameters, and FusedLayerNormModulate passing 1 + scale as the weight and
+ * shift as the bias of one layer-norm call).
+ */
+void oracle_layer_norm_modulate(const double *x, const double *scale, const double *shift,
+                                int64_t B, int64_t L, int64_t C, double eps, double *y) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < B * L; ++r) {
+        const int64_t b = r / L;
+        const double *xr = x + r * C;
+        double *yr = y + r * C;
+        double sum = 0.0;
+        for (int64_t c = 0; c < C; ++c) sum += xr[c];
+        const double mu = sum / (double)C;
+        double ss = 0.0;
+        for (int64_t c = 0; c < C; ++c) ss += (xr[c] - mu) * (xr[c] - mu);
+        const double inv = 1.0 / sqrt(ss / (double)C + eps);
+        for (int64_t c = 0; c < C; ++c) {
+            const double sc = scale ? scale[b * C + c] : 0.0, sh = shift ? shift[b * C + c] : 0.0;
+            yr[c] = (xr[c] - mu) * inv * (1.0 + sc) + sh;
+        }
     }
 }
 
@@ -101,18 +135,20 @@ void oracle_qk_norm_rope(const double *x, const double *w, const double *cos_tab
 
 /*
  * Attention of query rows `rows[0..nrows)` (all Sq rows when rows == NULL)
- * over the keys j in [kv_begin, kv_end):
+ * over the keys j in [kv_begin, kv_end) -- with `causal`, only keys j <= i
+ * (query index i; top-left aligned, as an is_causal scaled-dot-product
+ * attention masks):
  *   s_j  = scale * sum_d q_d k_{j,d}
  *   m    = max_j s_j,  l = sum_j exp(s_j - m)
  *   o    = sum_j exp(s_j - m) v_j / l
  *   lse  = m + ln l                    (natural log, scale included)
- * An empty key range gives o = 0 and lse = -inf.
+ * A row with no visible key gives o = 0 and lse = -inf.
  * Outputs: o [B, nrows, H, D], lse [B, H, nrows].
  */
-void oracle_attention(const double *q, const double *k, const double *v,
-                      int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t D,
-                      double scale, int64_t kv_begin, int64_t kv_end,
-                      const int64_t *rows, int64_t nrows, double *o, double *lse) {
+void oracle_attention_masked(const double *q, const double *k, const double *v,
+                             int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t D,
+                             double scale, int64_t kv_begin, int64_t kv_end, int causal,
+                             const int64_t *rows, int64_t nrows, double *o, double *lse) {
     if (rows == NULL) nrows = Sq;
     const int64_t n = kv_end - kv_begin;
     const int64_t total = B * H * nrows;
@@ -130,8 +166,15 @@ void oracle_attention(const double *q, const double *k, const double *v,
                 lse[(b * H + h) * nrows + r] = -INFINITY;
                 continue;
             }
+            /* keys visible to this row: all of the range, or (causal) those at index <= qi */
+            int64_t nv = n;
+            if (causal) nv = qi - kv_begin + 1 < n ? qi - kv_begin + 1 : n;
+            if (nv <= 0) {
+                lse[(b * H + h) * nrows + r] = -INFINITY;
+                continue;
+            }
             double m = -INFINITY;
-            for (int64_t j = 0; j < n; ++j) {
+            for (int64_t j = 0; j < nv; ++j) {
                 const double *kr = k + ((b * Skv + kv_begin + j) * H + h) * D;
                 double dot = 0.0;
                 for (int64_t d = 0; d < D; ++d) dot += qr[d] * kr[d];
@@ -139,7 +182,7 @@ void oracle_attention(const double *q, const double *k, const double *v,
                 if (sc[j] > m) m = sc[j];
             }
             double l = 0.0;
-            for (int64_t j = 0; j < n; ++j) {
+            for (int64_t j = 0; j < nv; ++j) {
                 double p = exp(sc[j] - m);
                 const double *vr = v + ((b * Skv + kv_begin + j) * H + h) * D;
                 for (int64_t d = 0; d < D; ++d) orow[d] += p * vr[d];
@@ -150,6 +193,13 @@ void oracle_attention(const double *q, const double *k, const double *v,
         }
         free(sc);
     }
+}
+
+void oracle_attention(const double *q, const double *k, const double *v,
+                      int64_t B, int64_t H, int64_t Sq, int64_t Skv, int64_t D,
+                      double scale, int64_t kv_begin, int64_t kv_end,
+                      const int64_t *rows, int64_t nrows, double *o, double *lse) {
+    oracle_attention_masked(q, k, v, B, H, Sq, Skv, D, scale, kv_begin, kv_end, 0, rows, nrows, o, lse);
 }
 
 /* Softmax probabilities P[b, h, i, j] = exp(s_ij - m_i) / l_i over keys [kv_begin, kv_end) (tiny shapes only). */

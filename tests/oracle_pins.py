@@ -78,6 +78,33 @@ def pin_rms_unit_rms(orc):
     _close(orc.rms_norm(7.5 * x, np.ones(32), 0.0), y, what="scale invariance")
 
 
+# ---------------------------------------------------------------- LayerNorm + modulation
+
+def pin_ln_modulate_torch(orc):
+    """Agrees with torch fp64 layer_norm using weight 1 + scale and bias shift, per sample."""
+    rng = _rng(23)
+    B, L, C = 3, 5, 24
+    x = rng.normal(0.5, 2, (B, L, C))
+    scale = rng.normal(0, 0.3, (B, C))
+    shift = rng.normal(0, 0.3, (B, C))
+    y = orc.layer_norm_modulate(x, scale, shift, 1e-6)
+    for b in range(B):
+        ref = torch.nn.functional.layer_norm(torch.from_numpy(x[b]), (C,), weight=torch.from_numpy(1 + scale[b]),
+                                             bias=torch.from_numpy(shift[b]), eps=1e-6).numpy()
+        _close(y[b], ref, rtol=1e-11, atol=1e-12, what="ln modulate vs torch")
+    plain = orc.layer_norm_modulate(x, None, None, 1e-6)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (C,), eps=1e-6).numpy()
+    _close(plain, ref, rtol=1e-11, atol=1e-12, what="plain ln vs torch")
+
+
+def pin_ln_modulate_closed_forms(orc):
+    """A constant row normalises to 0 (y = shift); x = (1, 3) has mean 2, variance 1."""
+    y = orc.layer_norm_modulate(np.full((1, 2, 4), 7.0), np.full((1, 4), 0.5), np.array([[1.0, -2.0, 0.0, 3.0]]), 1e-6)
+    _close(y, np.broadcast_to([1.0, -2.0, 0.0, 3.0], y.shape), what="constant row")
+    y = orc.layer_norm_modulate(np.array([[[1.0, 3.0]]]), np.array([[1.0, 0.0]]), np.array([[0.0, 10.0]]), 0.0)
+    _close(y.ravel(), [-2.0, 11.0], what="two-element row")
+
+
 # ---------------------------------------------------------------- RoPE
 
 def _angles_tables(theta):
@@ -272,6 +299,39 @@ def pin_attn_rows(orc):
     os_, ls = orc.attention(q, k, v, 0.5, rows=rows)
     _close(os_, o[:, rows], what="rows o")
     _close(ls, lse[:, :, rows], what="rows lse")
+
+
+def pin_attn_causal_sdpa(orc):
+    """causal: torch fp64 scaled_dot_product_attention(is_causal=True), square and rectangular."""
+    rng = _rng(21)
+    for B, H, Sq, Skv in [(2, 3, 9, 9), (1, 2, 6, 11), (1, 1, 12, 5)]:
+        q = rng.normal(0, 1, (B, Sq, H, 8))
+        k = rng.normal(0, 1, (B, Skv, H, 8))
+        v = rng.normal(0, 1, (B, Skv, H, 8))
+        o, lse = orc.attention(q, k, v, 0.45, causal=True)
+        tq, tk, tv = (torch.from_numpy(a).permute(0, 2, 1, 3) for a in (q, k, v))
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.45, is_causal=True)
+        mask = torch.ones(Sq, Skv, dtype=torch.bool).tril()
+        sc = (0.45 * (tq @ tk.transpose(-1, -2))).masked_fill(~mask, float("-inf"))
+        _close(o, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12, what="causal vs sdpa")
+        _close(lse, torch.logsumexp(sc, dim=-1).numpy(), rtol=1e-12, what="causal lse")
+
+
+def pin_attn_causal_first_row_and_chunks(orc):
+    """Row 0 sees only key 0; a chunk starting after a row gives it o = 0, lse = -inf; chunks merge to causal."""
+    rng = _rng(22)
+    q = rng.normal(0, 1, (1, 10, 2, 8))
+    k = rng.normal(0, 1, (1, 10, 2, 8))
+    v = rng.normal(0, 1, (1, 10, 2, 8))
+    o, lse = orc.attention(q, k, v, 0.3, causal=True)
+    _close(o[:, 0], v[:, 0], what="causal row 0")
+    _close(lse[:, :, 0], 0.3 * np.einsum("bhd,bhd->bh", q[:, 0], k[:, 0]), what="causal row 0 lse")
+    oc, lc = orc.attention(q, k, v, 0.3, 4, 10, causal=True)
+    assert np.all(oc[:, :4] == 0) and np.all(lc[:, :, :4] == -np.inf)
+    parts = [orc.attention(q, k, v, 0.3, lo, hi, causal=True) for lo, hi in [(0, 4), (4, 7), (7, 10)]]
+    om, lm = orc.merge_lse(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    _close(om, o, rtol=1e-10, atol=1e-12, what="causal chunks merged")
+    _close(lm, lse, rtol=1e-12, what="causal chunks merged lse")
 
 
 # ---------------------------------------------------------------- merge

@@ -132,6 +132,20 @@ def test_merge_empty_is_ok(lib):
     assert _merge(lib, Sq=0) == ops.DIT_OK
 
 
+@pytest.mark.parametrize("C,code", [(12, ops.DIT_ERR_UNSUPPORTED), (8200, ops.DIT_ERR_UNSUPPORTED),
+                                    (64, ops.DIT_OK)])
+def test_norm_entry_points_check_channels(lib, C, code):
+    # B = 0 makes the valid case empty work (no launch)
+    assert lib.dit_layer_norm_modulate(A16, None, None, A16 * 2, 0 if code == ops.DIT_OK else 1, 4, C, 1e-6,
+                                       None) == code
+    assert lib.dit_rms_norm(A16, A16 * 4, A16 * 2, 0 if code == ops.DIT_OK else 4, C, 1e-6, None) == code
+
+
+def test_norm_rejects_overlap(lib):
+    assert lib.dit_layer_norm_modulate(A16, None, None, A16 + 64, 1, 4, 64, 1e-6, None) == ops.DIT_ERR_INVALID_ARG
+    assert lib.dit_rms_norm(A16, A16 * 4, A16 + 64, 4, 64, 1e-6, None) == ops.DIT_ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
 

@@ -219,3 +219,68 @@ def test_bounded_wait_times_out_and_context_survives():
     q, k, v, *_ = inputs.small_case(1, 128, 1, 64, seed=5)
     o, _ = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v))
     assert torch.isfinite(o.float()).all()
+
+
+# ---------------------------------------------------------------- causal variant
+
+@pytest.mark.parametrize("B,H,Sq,Skv,D", [(1, 2, 256, 256, 64), (2, 3, 200, 333, 128), (1, 1, 517, 300, 128),
+                                          (1, 2, 700, 700, 128), (1, 1, 1, 1, 64)])
+def test_attn_fwd_causal_parity(orc, B, H, Sq, Skv, D):
+    q, k, v, *_ = inputs.small_case(B, Sq, H, D, seed=Sq + 3 * Skv, Skv=Skv, k_std=2.0)
+    o, lse = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v), o_dtype=torch.float32, causal=True)
+    f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+    ro, rl = orc.attention(*f, 1 / math.sqrt(D), causal=True)
+    check_o(host_f64(o), ro, f32=True, what=f"causal {B, H, Sq, Skv, D}", vmax=vmax(v))
+    check_lse(host_f64(lse), rl, what=f"causal {B, H, Sq, Skv, D}")
+
+
+def test_attn_fwd_causal_chunks_merge(orc):
+    """Causal key chunks: rows before a chunk see nothing (O = 0, LSE = -inf); merged chunks = full causal."""
+    B, H, S, D = 1, 2, 600, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=61)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    bounds = [(0, 150), (150, 389), (389, 600)]
+    o_parts = torch.empty((3, B, S, H, D), dtype=torch.float32, device="cuda")
+    lse_parts = torch.empty((3, B, H, S), dtype=torch.float32, device="cuda")
+    f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+    for c, (lo, hi) in enumerate(bounds):
+        ops.attn_fwd(tq, tk, tv, None, lo, hi, o=o_parts[c], lse=lse_parts[c], causal=True)
+        ro, rl = orc.attention(*f, 1 / math.sqrt(D), lo, hi, causal=True)
+        got_l = host_f64(lse_parts[c])
+        assert np.array_equal(np.isinf(got_l), np.isinf(rl))
+        assert np.all(host_f64(o_parts[c])[:, :lo] == 0)
+        fin = np.isfinite(rl)
+        assert np.abs(got_l[fin] - rl[fin]).max() <= 1e-3
+        check_o(host_f64(o_parts[c])[:, lo:], ro[:, lo:], f32=True, what=f"causal chunk {lo, hi}", vmax=vmax(v))
+    om, lm = ops.attn_merge_lse(o_parts, lse_parts, out_dtype=torch.float32)
+    ro, rl = orc.attention(*f, 1 / math.sqrt(D), causal=True)
+    check_o(host_f64(om), ro, f32=True, what="causal merged", vmax=vmax(v))
+    check_lse(host_f64(lm), rl, what="causal merged")
+
+
+# ---------------------------------------------------------------- LayerNorm-modulate / RMSNorm over C
+
+@pytest.mark.parametrize("B,L,C", [(2, 37, 3072), (1, 130, 5120), (3, 5, 8), (1, 7, 8192), (2, 300, 128)])
+def test_layer_norm_modulate_parity(orc, B, L, C):
+    rng = np.random.default_rng(C + L)
+    x = inputs.bf16_normal(B * L * C, seed=C + 7, std=2.0, mean=0.3).reshape(B, L, C)
+    scale = rng.normal(0, 0.3, (B, C)).astype(np.float32)
+    shift = rng.normal(0, 0.3, (B, C)).astype(np.float32)
+    y = ops.layer_norm_modulate(dev_bf16(x), dev_f32(scale), dev_f32(shift), 1e-6)
+    ref = orc.layer_norm_modulate(inputs.bf16_bits_to_f64(x), scale.astype(np.float64), shift.astype(np.float64), 1e-6)
+    check_bf16_rounding(host_f64(y), ref, "ln modulate", atol=2e-5)
+    y0 = ops.layer_norm_modulate(dev_bf16(x), None, None, 1e-6)
+    ref0 = orc.layer_norm_modulate(inputs.bf16_bits_to_f64(x), None, None, 1e-6)
+    check_bf16_rounding(host_f64(y0), ref0, "plain ln", atol=2e-5)
+
+
+@pytest.mark.parametrize("rows,C", [(37, 5120), (300, 3072), (1, 8)])
+def test_rms_norm_over_channels_parity(orc, rows, C):
+    x = inputs.bf16_normal(rows * C, seed=rows + C).reshape(rows, C)
+    w = inputs.f32_normal(C, seed=C, std=0.1, mean=1.0)
+    tx = dev_bf16(x)
+    y = ops.rms_norm(tx, dev_f32(w), 1e-6)
+    ref = orc.rms_norm(inputs.bf16_bits_to_f64(x), w.astype(np.float64), 1e-6)
+    check_bf16_rounding(host_f64(y), ref, "rms over C")
+    ops.rms_norm(tx, dev_f32(w), 1e-6, y=tx)  # in place
+    assert torch.equal(tx, y)

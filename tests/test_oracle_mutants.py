@@ -29,6 +29,13 @@ MUTANTS = {
     "attn_no_normalise": ("for (int64_t d = 0; d < D; ++d) orow[d] /= l;", ""),
     "attn_ignores_begin": ("const double *vr = v + ((b * Skv + kv_begin + j) * H + h) * D;",
                            "const double *vr = v + ((b * Skv + j) * H + h) * D;"),
+    "causal_strict": ("if (causal) nv = qi - kv_begin + 1 < n ? qi - kv_begin + 1 : n;",
+                      "if (causal) nv = qi - kv_begin < n ? qi - kv_begin : n;"),
+    "causal_ignores_begin": ("if (causal) nv = qi - kv_begin + 1 < n ? qi - kv_begin + 1 : n;",
+                             "if (causal) nv = qi + 1 < n ? qi + 1 : n;"),
+    "ln_unbiased_var": ("const double inv = 1.0 / sqrt(ss / (double)C + eps);",
+                        "const double inv = 1.0 / sqrt(ss / (double)(C - 1) + eps);"),
+    "ln_scale_not_plus_one": ("yr[c] = (xr[c] - mu) * inv * (1.0 + sc) + sh;", "yr[c] = (xr[c] - mu) * inv * sc + sh;"),
     "merge_weight_vs_max": ("double wgt = exp(lse_parts[c * part_l + li] - L);",
                             "double wgt = exp(lse_parts[c * part_l + li] - mx);"),
     "merge_lse_drops_max": ("double L = mx + log(sum);", "double L = log(sum);"),
