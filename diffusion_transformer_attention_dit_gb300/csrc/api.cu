@@ -193,7 +193,7 @@ dit_status dit_layer_norm_modulate(const void *x, const float *scale, const floa
   if (!(eps >= 0.f) || isinf(eps)) return fail(DIT_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if ((int64_t)B * L * C == 0) return DIT_OK;
   if (!x || !y) return fail(DIT_ERR_INVALID_ARG, "null pointer");
-  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(scale, 4) || !aligned(shift, 4))
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(scale, 16) || !aligned(shift, 16))
     return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
   const uintptr_t n = (uintptr_t)B * L * C * 2;
   const Range rx = {reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + n};
@@ -213,7 +213,7 @@ dit_status dit_rms_norm(const void *x, const float *w, void *y, int64_t rows, in
   if (!(eps >= 0.f) || isinf(eps)) return fail(DIT_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (rows * C == 0) return DIT_OK;
   if (!x || !y || !w) return fail(DIT_ERR_INVALID_ARG, "null pointer");
-  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 4)) return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 16)) return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
   const uintptr_t n = (uintptr_t)rows * C * 2;
   const Range rx = {reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + n};
   const Range ry = {reinterpret_cast<uintptr_t>(y), reinterpret_cast<uintptr_t>(y) + n};

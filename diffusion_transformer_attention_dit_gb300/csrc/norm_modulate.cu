@@ -10,10 +10,11 @@
 // WanRMSNorm on [B, L, C]):   y = x * w / sqrt(mean(x^2) + eps)
 // fp32 arithmetic, one bf16 rounding.
 //
-// HBM-bound (2 bytes read + 2 written per element).  One CTA of 128 threads
-// per row (grid-stride beyond 2^31 rows); the row sits in registers as 16-byte
-// vectors (C <= 8192, C a multiple of 8), so the two passes (mean, then the
-// squared deviations) read HBM once.
+// HBM-bound (2 bytes read + 2 written per element).  A row is spread over 128
+// threads as 16-byte vectors held in registers (C <= 8192, C a multiple of 8),
+// so the two passes (mean, then the squared deviations) read HBM once.
+// Persistent CTAs (8 per SM) issue the next row's loads before reducing the
+// current one.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,90 +32,152 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Sum over the CTA; every thread gets the result.  `red` holds 4 floats.
+// Sum over the CTA; every thread gets the result.  `red` holds 4 floats.  One
+// barrier per call: the callers alternate between two `red` buffers, and the
+// barrier of the next call on the other buffer orders each buffer's reads
+// before its next writes.
 __device__ __forceinline__ float block_sum(float v, float *red) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  __syncthreads();  // `red` may still be read from the previous reduction
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   return (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-template <bool kLayerNorm>
+// Normalise one row whose 16-byte vectors this thread holds in `raw`, and store it.
+template <bool kLayerNorm, int kVec>
+__device__ __forceinline__ void norm_row(const uint4 (&raw)[kVec], uint4 *y, const float *__restrict__ a,
+                                         const float *__restrict__ c, long long r, int nvec, int C, int L, float eps,
+                                         float *red) {
+  const float inv_c = 1.0f / C;
+  float v[kVec][8];
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const uint32_t ww[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[u][2 * e] = __uint_as_float(ww[e] << 16);
+      v[u][2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+    }
+  }
+  float inv, mu = 0.f;
+  if (kLayerNorm) {
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < kVec; ++u)
+      if (threadIdx.x + u * kThreads < nvec)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += v[u][e];
+    mu = block_sum(s, red) * inv_c;
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < kVec; ++u)
+      if (threadIdx.x + u * kThreads < nvec)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[u][e] - mu, v[u][e] - mu, ss);
+    inv = rsqrtf(fmaf(block_sum(ss, red + 4), inv_c, eps));
+  } else {
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < kVec; ++u)
+      if (threadIdx.x + u * kThreads < nvec)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[u][e], v[u][e], ss);
+    inv = rsqrtf(fmaf(block_sum(ss, red), inv_c, eps));  // the caller alternates `red` between rows
+  }
+  // LayerNorm: a = scale [B, C], c = shift [B, C] (either may be null); RMSNorm: a = weight [C].
+  // The per-channel factors are read as two 16-byte vectors per 8 channels.
+  const long long arow = kLayerNorm ? (r / L) * C : 0;
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    if (i < nvec) {
+      float fa[8], fc[8];
+      if (a) {
+        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(a + arow) + 2 * i);
+        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(a + arow) + 2 * i + 1);
+        fa[0] = a0.x, fa[1] = a0.y, fa[2] = a0.z, fa[3] = a0.w, fa[4] = a1.x, fa[5] = a1.y, fa[6] = a1.z, fa[7] = a1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) fa[e] = 0.f;
+      }
+      if (kLayerNorm && c) {
+        const float4 c0 = __ldg(reinterpret_cast<const float4 *>(c + arow) + 2 * i);
+        const float4 c1 = __ldg(reinterpret_cast<const float4 *>(c + arow) + 2 * i + 1);
+        fc[0] = c0.x, fc[1] = c0.y, fc[2] = c0.z, fc[3] = c0.w, fc[4] = c1.x, fc[5] = c1.y, fc[6] = c1.z, fc[7] = c1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) fc[e] = 0.f;
+      }
+      uint32_t out[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float o2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ch = 2 * e + h;
+          o2[h] = kLayerNorm ? (v[u][ch] - mu) * inv * (1.0f + fa[ch]) + fc[ch] : v[u][ch] * inv * fa[ch];
+        }
+        out[e] = pack_bf16(o2[0], o2[1]);
+      }
+      __stcs(y + r * nvec + i, make_uint4(out[0], out[1], out[2], out[3]));
+    }
+  }
+}
+
+template <int kVec>
+__device__ __forceinline__ void load_row(uint4 (&raw)[kVec], const uint4 *__restrict__ x, long long r, int nvec) {
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    if (i < nvec) raw[u] = __ldcs(x + r * nvec + i);
+  }
+}
+
+// Persistent CTAs walk rows r = blockIdx.x, + gridDim.x, ...; the next row's
+// loads are issued before the current row's reductions, so two rows per CTA
+// are in flight.
+template <bool kLayerNorm, int kVec>
 __global__ void __launch_bounds__(kThreads) row_norm_kernel(const uint4 *__restrict__ x, uint4 *y,
                                                             const float *__restrict__ a, const float *__restrict__ c,
                                                             long long rows, int C, int L, float eps) {
-  __shared__ float red[4];
+  __shared__ float red[8];
   const int nvec = C / 8;
-  const float inv_c = 1.0f / C;
-  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
-    const uint4 *xr = x + r * nvec;
-    float v[kMaxVec][8];
-#pragma unroll
-    for (int u = 0; u < kMaxVec; ++u) {
-      const int i = threadIdx.x + u * kThreads;
-      if (i < nvec) {
-        const uint4 w = __ldcs(xr + i);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[u][2 * e] = __uint_as_float(ww[e] << 16);
-          v[u][2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
-        }
-      }
-    }
-    float inv, mu = 0.f;
-    if (kLayerNorm) {
-      float s = 0.f;
-#pragma unroll
-      for (int u = 0; u < kMaxVec; ++u)
-        if (threadIdx.x + u * kThreads < nvec)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) s += v[u][e];
-      mu = block_sum(s, red) * inv_c;
-      float ss = 0.f;
-#pragma unroll
-      for (int u = 0; u < kMaxVec; ++u)
-        if (threadIdx.x + u * kThreads < nvec)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ss = fmaf(v[u][e] - mu, v[u][e] - mu, ss);
-      inv = rsqrtf(fmaf(block_sum(ss, red), inv_c, eps));
-    } else {
-      float ss = 0.f;
-#pragma unroll
-      for (int u = 0; u < kMaxVec; ++u)
-        if (threadIdx.x + u * kThreads < nvec)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ss = fmaf(v[u][e], v[u][e], ss);
-      inv = rsqrtf(fmaf(block_sum(ss, red), inv_c, eps));
-    }
-    // LayerNorm: a = scale [B, C], c = shift [B, C] (either may be null); RMSNorm: a = weight [C]
-    const long long arow = kLayerNorm ? (r / L) * C : 0;
-#pragma unroll
-    for (int u = 0; u < kMaxVec; ++u) {
-      const int i = threadIdx.x + u * kThreads;
-      if (i < nvec) {
-        uint32_t out[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float o2[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int ch = i * 8 + 2 * e + h;
-            if (kLayerNorm) {
-              const float sc = a ? a[arow + ch] : 0.f, sh = c ? c[arow + ch] : 0.f;
-              o2[h] = (v[u][2 * e + h] - mu) * inv * (1.0f + sc) + sh;
-            } else {
-              o2[h] = v[u][2 * e + h] * inv * a[ch];
-            }
-          }
-          out[e] = pack_bf16(o2[0], o2[1]);
-        }
-        y[r * nvec + i] = make_uint4(out[0], out[1], out[2], out[3]);
-      }
-    }
+  uint4 cur[kVec], nxt[kVec];
+  long long r = blockIdx.x;
+  if (r < rows) load_row<kVec>(cur, x, r, nvec);
+  for (; r < rows; r += 2LL * gridDim.x) {
+    const long long r1 = r + gridDim.x;
+    if (r1 < rows) load_row<kVec>(nxt, x, r1, nvec);
+    // LayerNorm rows use red[0..3] and red[4..7] (two barriers per row); RMSNorm
+    // rows (one barrier each) alternate between them
+    norm_row<kLayerNorm, kVec>(cur, y, a, c, r, nvec, C, L, eps, red);
+    if (r1 >= rows) break;
+    const long long r2 = r1 + gridDim.x;
+    if (r2 < rows) load_row<kVec>(cur, x, r2, nvec);
+    norm_row<kLayerNorm, kVec>(nxt, y, a, c, r1, nvec, C, L, eps, kLayerNorm ? red : red + 4);
   }
+}
+
+template <bool kLayerNorm>
+cudaError_t launch_rows(const void *x, const float *a, const float *c, void *y, long long rows, int C, int L,
+                        float eps, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long cap = 8LL * sms;  // persistent CTAs
+  const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
+  const int nvec = C / 8;
+  const uint4 *xx = static_cast<const uint4 *>(x);
+  uint4 *yy = static_cast<uint4 *>(y);
+  if (nvec <= 2 * kThreads)
+    row_norm_kernel<kLayerNorm, 2><<<grid, kThreads, 0, stream>>>(xx, yy, a, c, rows, C, L, eps);
+  else if (nvec <= 4 * kThreads)
+    row_norm_kernel<kLayerNorm, 4><<<grid, kThreads, 0, stream>>>(xx, yy, a, c, rows, C, L, eps);
+  else
+    row_norm_kernel<kLayerNorm, kMaxVec><<<grid, kThreads, 0, stream>>>(xx, yy, a, c, rows, C, L, eps);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -123,19 +186,12 @@ int row_norm_max_channels() { return kMaxVec * 8 * kThreads; }
 
 cudaError_t launch_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y, int B, int L,
                                        int C, float eps, cudaStream_t stream) {
-  const long long rows = (long long)B * L;
-  const long long grid = rows < 0x7fffffffLL ? rows : 0x7fffffffLL;
-  row_norm_kernel<true><<<(unsigned)grid, kThreads, 0, stream>>>(static_cast<const uint4 *>(x), static_cast<uint4 *>(y),
-                                                                 scale, shift, rows, C, L, eps);
-  return cudaGetLastError();
+  return launch_rows<true>(x, scale, shift, y, (long long)B * L, C, L, eps, stream);
 }
 
 cudaError_t launch_rms_norm(const void *x, const float *w, void *y, long long rows, int C, float eps,
                             cudaStream_t stream) {
-  const long long grid = rows < 0x7fffffffLL ? rows : 0x7fffffffLL;
-  row_norm_kernel<false><<<(unsigned)grid, kThreads, 0, stream>>>(static_cast<const uint4 *>(x),
-                                                                  static_cast<uint4 *>(y), w, nullptr, rows, C, 1, eps);
-  return cudaGetLastError();
+  return launch_rows<false>(x, w, nullptr, y, rows, C, 1, eps, stream);
 }
 
 }  // namespace ditattn

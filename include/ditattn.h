@@ -179,7 +179,7 @@ dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const flo
  * with the biased variance; fp32 arithmetic, one bf16 rounding.
  *
  *   x, y           bf16 [B, L, C], contiguous, 16-byte aligned; y may equal x
- *   scale, shift   fp32 [B, C] (one modulation vector per sample), or NULL for 0
+ *   scale, shift   fp32 [B, C] (one modulation vector per sample), 16-byte aligned, or NULL for 0
  *   C              a multiple of 8, at most 8192 (else DIT_ERR_UNSUPPORTED)
  */
 dit_status dit_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y,
@@ -195,7 +195,7 @@ dit_status dit_layer_norm_modulate(const void *x, const float *scale, const floa
  * whole-token variant.
  *
  *   x, y   bf16 [rows, C], contiguous, 16-byte aligned; y may equal x
- *   w      fp32 [C]
+ *   w      fp32 [C], 16-byte aligned
  *   C      a multiple of 8, at most 8192
  */
 dit_status dit_rms_norm(const void *x, const float *w, void *y, int64_t rows, int C, float eps,
