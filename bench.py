@@ -382,6 +382,57 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_ring_overlap(args):
+    """Diagnostic: the ring-overlap emulation (local attention || gather of the remote key shards, attention over
+    the gathered keys, merge) against the same steps run back to back on one stream."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import build, ops
+
+    build.build()
+    ops.load_library()
+    inp = inputs.make_inputs(args.workload)
+    w = inp.w
+    dev = torch.device("cuda")
+    q, k, v = (torch.from_numpy(np.ascontiguousarray(getattr(inp, n)).view(np.int16)).to(dev).view(torch.bfloat16)
+               for n in ("q", "k", "v"))
+    bounds = w.chunk_bounds(args.ring_overlap)
+    k_loc, v_loc = k[:, :bounds[0][1]].contiguous(), v[:, :bounds[0][1]].contiguous()
+    remote = [(k[:, lo:hi].contiguous(), v[:, lo:hi].contiguous()) for lo, hi in bounds[1:]]
+    side = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def serial():
+        kr = torch.cat([a for a, _ in remote], dim=1)
+        vr = torch.cat([b for _, b in remote], dim=1)
+        o1, l1 = ops.attn_fwd(q, k_loc, v_loc, o_dtype=torch.float32)
+        o2, l2 = ops.attn_fwd(q, kr, vr, o_dtype=torch.float32)
+        return ops.attn_merge_lse(torch.stack([o1, o2]), torch.stack([l1, l2]))
+
+    def overlapped():
+        return ops.ring_overlap_attention(q, k_loc, v_loc, remote, gather_stream=side)
+
+    res = {}
+    for name, fn in (("serial", serial), ("overlapped", overlapped)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(args.steps, 5)):
+            flush.zero_()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        res[name] = statistics.median(ts)
+    print(json.dumps({"mode": "ring_overlap_emulation", "workload": w.name, "ranks": args.ring_overlap,
+                      "serial_ms": res["serial"], "overlapped_ms": res["overlapped"],
+                      "attention_tflops_overlapped": w.attention_flops() / res["overlapped"] / 1e9}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,6 +444,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=48, help="query rows per (b, h) in each reference step")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ring-overlap", type=int, default=0, metavar="RANKS",
+                    help="time the one-GPU ring-overlap emulation with RANKS key shards instead (diagnostic)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -402,6 +455,8 @@ def main():
         args.steps = 5
     if args.impl == "reference":
         run_reference(args)
+    elif args.ring_overlap:
+        run_ring_overlap(args)
     else:
         run_ours(args)
 

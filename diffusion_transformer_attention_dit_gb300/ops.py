@@ -224,3 +224,34 @@ def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1,
     for c in range(chunks):
         attn_fwd(q, k, v, scale, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c], stream=stream)
     return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype, stream=stream)
+
+
+def ring_overlap_attention(q, k_local, v_local, remote_kv, scale: float | None = None, out_dtype=torch.bfloat16,
+                           partial_dtype=torch.float32, gather_stream=None):
+    """Two-attention ring overlap on one GPU ("NPU Wan2.2-I2V model inference optimisation
+    practice", section "Ring Attention Overlap").
+
+    Attention over the local K/V runs on the current stream while the remote K/V
+    chunks are gathered into one contiguous buffer on `gather_stream` (device
+    copies stand in for the all-gather of a multi-GPU run); then one attention
+    over the gathered chunks and an LSE merge of the two results.  remote_kv is
+    a list of (k_i, v_i) tensors [B, S_i, H, D].  Returns (o, lse).
+    """
+    main = torch.cuda.current_stream()
+    side = gather_stream if gather_stream is not None else torch.cuda.Stream(device=q.device)
+    B, Sq, H, D = q.shape
+    side.wait_stream(main)  # the remote chunks must be ready before they are copied
+    with torch.cuda.stream(side):
+        k_r = torch.cat([kk for kk, _ in remote_kv], dim=1)
+        v_r = torch.cat([vv for _, vv in remote_kv], dim=1)
+        gathered = torch.cuda.Event()
+        gathered.record(side)
+    k_r.record_stream(main)
+    v_r.record_stream(main)
+    o_parts = torch.empty((2, B, Sq, H, D), dtype=partial_dtype, device=q.device)
+    lse_parts = torch.empty((2, B, H, Sq), dtype=torch.float32, device=q.device)
+    attn_fwd(q, k_local, v_local, scale, o=o_parts[0], lse=lse_parts[0])
+    main.wait_event(gathered)
+    attn_fwd(q, k_r, v_r, scale, o=o_parts[1], lse=lse_parts[1])
+    return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype)
+

@@ -284,3 +284,19 @@ def test_rms_norm_over_channels_parity(orc, rows, C):
     check_bf16_rounding(host_f64(y), ref, "rms over C")
     ops.rms_norm(tx, dev_f32(w), 1e-6, y=tx)  # in place
     assert torch.equal(tx, y)
+
+
+# ---------------------------------------------------------------- ring-overlap emulation
+
+def test_ring_overlap_equals_full_attention(orc):
+    """Local FA || gather of 3 remote chunks on a side stream, FA over the gathered keys, LSE merge == full."""
+    B, H, S, D = 1, 4, 1000, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=91, k_std=2.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    bounds = [(0, 250), (250, 500), (500, 800), (800, 1000)]  # rank 0 local, ranks 1-3 remote
+    remote = [(tk[:, lo:hi].contiguous(), tv[:, lo:hi].contiguous()) for lo, hi in bounds[1:]]
+    o, lse = ops.ring_overlap_attention(tq, tk[:, :250].contiguous(), tv[:, :250].contiguous(), remote)
+    torch.cuda.synchronize()
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
+    check_o(host_f64(o), ro, what="ring overlap")
+    check_lse(host_f64(lse), rl, what="ring overlap")
