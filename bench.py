@@ -39,7 +39,7 @@ L2_FLUSH_BYTES = 512 << 20
 PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480": "f32", "wan720": "bf16"}
 # DRAM bytes per attention launch (read + write) from an ncu capture of the bench step
 # (profiles/launch_list_qwen_image_step.md), valid for the attention source it was taken on.
-ATTN_TRAFFIC = {"source_sha256_prefix": "b02eef41b2adeae0", "qwen_image": (39.0 + 55.8) * 1e6}
+ATTN_TRAFFIC = {"source_sha256_prefix": "9fcb952b8c9608e4", "qwen_image": (39.3 + 56.2) * 1e6}
 
 
 def peaks():
