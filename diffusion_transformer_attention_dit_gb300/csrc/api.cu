@@ -179,8 +179,10 @@ dit_status dit_poll_device_error(struct CUstream_st *stream) {
   if (e == cudaSuccess) e = ditattn::read_and_clear_attn_error(&va);
   if (e == cudaSuccess) e = ditattn::read_and_clear_prologue_error(&vp);
   if (e == cudaSuccess) e = ditattn::read_and_clear_merge_error(&vm);
+  unsigned int vf = 0;
+  if (e == cudaSuccess) e = ditattn::read_and_clear_fp8_error(&vf);
   if (e != cudaSuccess) return from_cuda(e, nullptr);
-  if (va | vp | vm) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (va | vp | vm | vf) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return DIT_OK;
 }
 
@@ -219,6 +221,43 @@ dit_status dit_rms_norm(const void *x, const float *w, void *y, int64_t rows, in
   const Range ry = {reinterpret_cast<uintptr_t>(y), reinterpret_cast<uintptr_t>(y) + n};
   if (x != y && overlap(rx, ry)) return fail(DIT_ERR_INVALID_ARG, "y overlaps x (only exact in-place is allowed)");
   return from_cuda(ditattn::launch_rms_norm(x, w, y, rows, C, eps, reinterpret_cast<cudaStream_t>(stream)), nullptr);
+}
+
+dit_status dit_quant_fp8_rows(const void *x, void *codes, float *scale, int64_t M, int K, struct CUstream_st *stream) {
+  g_detail = "";
+  if (M < 0 || K < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if (K % 16 || K > ditattn::quant_fp8_max_k())
+    return fail(DIT_ERR_UNSUPPORTED, "K must be a multiple of 16 and at most 8192");
+  if (M * K == 0) return DIT_OK;
+  if (!x || !codes || !scale) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scale, 4)) return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const Range rx = {reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + (uintptr_t)M * K * 2};
+  const Range rc = {reinterpret_cast<uintptr_t>(codes), reinterpret_cast<uintptr_t>(codes) + (uintptr_t)M * K};
+  const Range rs = {reinterpret_cast<uintptr_t>(scale), reinterpret_cast<uintptr_t>(scale) + (uintptr_t)M * 4};
+  if (overlap(rx, rc) || overlap(rx, rs) || overlap(rc, rs)) return fail(DIT_ERR_INVALID_ARG, "buffers overlap");
+  return from_cuda(ditattn::launch_quant_fp8_rows(x, codes, scale, M, K, reinterpret_cast<cudaStream_t>(stream)),
+                   nullptr);
+}
+
+dit_status dit_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out, int M,
+                        int N, int K, int64_t lda, int64_t ldb, int64_t ldo, struct CUstream_st *stream) {
+  g_detail = "";
+  if (M < 0 || N < 0 || K < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
+  if ((int64_t)M * N == 0) return DIT_OK;
+  if (K <= 0 || K % 16) return fail(DIT_ERR_UNSUPPORTED, "K must be a positive multiple of 16");
+  if (!a || !b || !a_scale || !b_scale || !out) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  if (lda < K || ldb < K || ldo < N || lda % 16 || ldb % 16 || ldo % 8)
+    return fail(DIT_ERR_INVALID_ARG, "leading dimensions must cover a row and be multiples of 16 bytes");
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16) || !aligned(a_scale, 4) || !aligned(b_scale, 4))
+    return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+  const Range ro = {reinterpret_cast<uintptr_t>(out), reinterpret_cast<uintptr_t>(out) + (uintptr_t)((M - 1) * ldo + N) * 2};
+  const Range ra = {reinterpret_cast<uintptr_t>(a), reinterpret_cast<uintptr_t>(a) + (uintptr_t)((M - 1) * lda + K)};
+  const Range rb = {reinterpret_cast<uintptr_t>(b), reinterpret_cast<uintptr_t>(b) + (uintptr_t)((N - 1) * ldb + K)};
+  if (overlap(ro, ra) || overlap(ro, rb)) return fail(DIT_ERR_INVALID_ARG, "output overlaps an input");
+  const char *detail = nullptr;
+  cudaError_t e = ditattn::launch_gemm_fp8(a, a_scale, b, b_scale, out, M, N, K, lda, ldb, ldo,
+                                           reinterpret_cast<cudaStream_t>(stream), &detail);
+  return from_cuda(e, detail);
 }
 
 dit_status dit_selftest_wait_timeout(struct CUstream_st *stream) {

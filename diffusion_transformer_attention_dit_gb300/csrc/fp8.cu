@@ -1,0 +1,384 @@
+// W8A8 fp8 (e4m3) projection for GB300 (sm_103a): per-token dynamic
+// quantisation and the scaled fp8 GEMM that consumes it.
+//
+// Operation ("feat: support Ascend NPU backend (torch_npu) for Qwen-Image
+// pipelines - #274", item 4, npu_quant_linear: per-token dynamic activation
+// quantisation, per-channel weight scales, quantised matmul to bf16):
+//   quantise:  scale_m = max_k |x_mk| / 448 (1 for an all-zero row),
+//              code_mk = e4m3(x_mk / scale_m)   (round to nearest even, saturating)
+//   GEMM:      out_mn = a_scale_m * b_scale_n * sum_k A_mk B_nk
+//
+// Quantiser: HBM-bound; a row is spread over 128 threads as 16-byte vectors
+// held in registers, one CTA max-reduction per row; persistent CTAs issue the
+// next row's loads before reducing the current one; the quotient is formed
+// with IEEE division and converted with cvt.rn.satfinite.e4m3x2.
+//
+// GEMM: one CTA per 128 x 256 output tile.  A TMA warp streams 128-byte K
+// blocks of A (128 rows) and B (256 rows) into a 4-stage ring (128-byte
+// swizzle); one thread issues tcgen05.mma kind::f8f6f4 (M 128, N 256, K 32 per
+// instruction) into a 256-column fp32 TMEM accumulator; four epilogue warps
+// read it back, apply the two scales, convert to bf16, stage the tile in the
+// drained ring in swizzled layout and store it with TMA.  Waits are bounded.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace ditattn {
+namespace {
+
+__device__ unsigned int g_fp8_error = 0;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitLimitIters = 1u << 26;
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || i > kWaitLimitIters)) {
+      atomicOr(&g_fp8_error, 1u);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- quantiser
+
+constexpr int kQThreads = 128;
+constexpr int kQMaxVec = 8;  // 16-byte bf16 vectors per thread: K <= 8192
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int kVec>
+__device__ __forceinline__ void q_load_row(uint4 (&raw)[kVec], const uint4 *__restrict__ x, long long m, int nvec) {
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const int i = threadIdx.x + u * kQThreads;
+    if (i < nvec) raw[u] = __ldcs(x + m * nvec + i);
+  }
+}
+
+// Quantise one row whose 16-byte vectors this thread holds in `raw`.  `red`
+// holds 4 floats; callers alternate two buffers between rows (one barrier each).
+template <int kVec>
+__device__ __forceinline__ void q_row(const uint4 (&raw)[kVec], uint2 *codes, float *scale, long long m, int nvec,
+                                      float *red) {
+  float v[kVec][8];
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const uint32_t ww[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[u][2 * e] = __uint_as_float(ww[e] << 16);
+      v[u][2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+    }
+    if (threadIdx.x + u * kQThreads < nvec)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[u][e]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (threadIdx.x == 0) scale[m] = sc;
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const int i = threadIdx.x + u * kQThreads;
+    if (i < nvec) {
+      uint32_t w[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint16_t lo = e4m3x2(__fdiv_rn(v[u][4 * e], sc), __fdiv_rn(v[u][4 * e + 1], sc));
+        const uint16_t hi = e4m3x2(__fdiv_rn(v[u][4 * e + 2], sc), __fdiv_rn(v[u][4 * e + 3], sc));
+        w[e] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+      __stcs(codes + m * nvec + i, make_uint2(w[0], w[1]));
+    }
+  }
+}
+
+// Persistent CTAs walk rows m = blockIdx.x, + gridDim.x, ...; the next row's
+// loads are issued before the current row's reduction.
+template <int kVec>
+__global__ void __launch_bounds__(kQThreads) quant_fp8_rows_kernel(const uint4 *__restrict__ x, uint2 *codes,
+                                                                   float *scale, long long M, int K) {
+  __shared__ float red[8];
+  const int nvec = K / 8;
+  uint4 cur[kVec], nxt[kVec];
+  long long m = blockIdx.x;
+  if (m < M) q_load_row<kVec>(cur, x, m, nvec);
+  for (; m < M; m += 2LL * gridDim.x) {
+    const long long m1 = m + gridDim.x;
+    if (m1 < M) q_load_row<kVec>(nxt, x, m1, nvec);
+    q_row<kVec>(cur, codes, scale, m, nvec, red);
+    if (m1 >= M) break;
+    const long long m2 = m1 + gridDim.x;
+    if (m2 < M) q_load_row<kVec>(cur, x, m2, nvec);
+    q_row<kVec>(nxt, codes, scale, m1, nvec, red + 4);
+  }
+}
+
+// ---------------------------------------------------------------- GEMM
+
+constexpr int kGM = 128, kGN = 256, kGK = 128;  // tile (K in bytes = elements)
+constexpr int kGStages = 4;
+constexpr int kGThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kABytes = kGM * kGK, kBBytes = kGN * kGK, kStageBytes = kABytes + kBBytes;
+constexpr int kBarOff = kGStages * kStageBytes;
+constexpr int kGNumBars = 2 * kGStages + 1;
+constexpr int kScaleOff = kBarOff + 8 * kGNumBars + 8;  // b_scale of the tile (256 floats)
+constexpr int kTmemSlotOff = kScaleOff + 4 * kGN;
+constexpr int kGSmem = kTmemSlotOff + 16 + 1024;
+
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                  /* D format: f32 */
+         | (0u << 7) | (0u << 10)                   /* A, B format: e4m3 */
+         | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ a_scale,
+                    const float *__restrict__ b_scale, int M, int N, int K) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *sbase = smem_raw + (base - raw);
+  float *s_bscale = reinterpret_cast<float *>(sbase + kScaleOff);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + kTmemSlotOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kGN, m0 = blockIdx.y * kGM;
+  const int nk = (K + kGK - 1) / kGK;
+  const uint32_t bars = base + kBarOff;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (kGStages + s); };
+  const uint32_t acc_full = bars + 8u * (2 * kGStages);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_fence_init();
+  }
+  if (warp >= 2)  // epilogue warps stage this tile's column scales
+    for (int i = threadIdx.x - 64; i < kGN; i += 128) s_bscale[i] = n0 + i < N ? b_scale[n0 + i] : 0.f;
+  if (warp == 1) {
+    tmem_alloc(base + kTmemSlotOff, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kGStages;
+        if (!wait_bounded(empty(s), ((kb / kGStages) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(full(s), kStageBytes);
+        tma_load_2d(base + s * kStageBytes, &tm_a, full(s), kb * kGK, m0);
+        tma_load_2d(base + s * kStageBytes + kABytes, &tm_b, full(s), kb * kGK, n0);
+        ++issued;
+      }
+      for (int i = issued > kGStages ? issued - kGStages : 0; i < issued; ++i)
+        wait_bounded(full(i % kGStages), (i / kGStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kGM, kGN);
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int s = kb % kGStages;
+        ok = wait_bounded(full(s), (kb / kGStages) & 1);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const uint32_t a0 = base + s * kStageBytes, b0 = a0 + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kGK / 32; ++kk)
+          mma_f8(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc,
+                 (kb > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(empty(s));
+      }
+      tc_commit(acc_full);  // also drains: every MMA issued has completed when this fires
+      wait_bounded(acc_full, 0);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 (one output row per thread)
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const bool ok = named_barrier_and(1, 128, wait_bounded(acc_full, 0));
+    if (ok) {
+      tc_fence_after_sync();
+      const float as = m0 + row < M ? a_scale[m0 + row] : 0.f;
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t sw = row & 7;
+      // the drained ring holds the bf16 tile: box c (64 columns) at c * 16 KB, 128-byte rows, swizzled
+#pragma unroll 1
+      for (int c = 0; c < kGN / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_x32(tmem + lane_base + c * 32, o);
+        const uint32_t dst = base + (c >> 1) * 16384 + row * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = c * 32 + 8 * u + 2 * e;
+            w[e] = pack_bf16(__uint_as_float(o[8 * u + 2 * e]) * as * s_bscale[col],
+                             __uint_as_float(o[8 * u + 2 * e + 1]) * as * s_bscale[col + 1]);
+          }
+          st_shared_v4(dst + ((((c & 1) * 4 + u) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
+      if (row == 0) {
+        for (int c = 0; c < kGN / 64; ++c)
+          if (n0 + c * 64 < N) tma_store_2d(&tm_o, base + c * 16384, n0 + c * 64, m0);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major map (inner dim first) with a box of box0 x box1 and 128-byte swizzle.
+bool encode_2d(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int esize, long long inner, long long outer,
+               long long ld_elems, int box0, int box1) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_elems * esize};
+  cuuint32_t box[2] = {(cuuint32_t)box0, (cuuint32_t)box1};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int quant_fp8_max_k() { return kQMaxVec * 8 * kQThreads; }
+
+cudaError_t launch_quant_fp8_rows(const void *x, void *codes, float *scale, long long M, int K, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long cap = 8LL * sms;  // persistent CTAs
+  const unsigned grid = static_cast<unsigned>(M < cap ? M : cap);
+  const uint4 *xx = static_cast<const uint4 *>(x);
+  uint2 *cc = static_cast<uint2 *>(codes);
+  const int nvec = K / 8;
+  if (nvec <= 2 * kQThreads)
+    quant_fp8_rows_kernel<2><<<grid, kQThreads, 0, stream>>>(xx, cc, scale, M, K);
+  else if (nvec <= 4 * kQThreads)
+    quant_fp8_rows_kernel<4><<<grid, kQThreads, 0, stream>>>(xx, cc, scale, M, K);
+  else
+    quant_fp8_rows_kernel<kQMaxVec><<<grid, kQThreads, 0, stream>>>(xx, cc, scale, M, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,
+                            int M, int N, int K, long long lda, long long ldb, long long ldo, cudaStream_t stream,
+                            const char **detail) {
+  CUtensorMap ta, tb, to;
+  if (!encode_2d(&ta, a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, M, lda, kGK, kGM) ||
+      !encode_2d(&tb, b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, ldb, kGK, kGN) ||
+      !encode_2d(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, M, ldo, 64, kGM)) {
+    *detail = "cuTensorMapEncodeTiled failed for the fp8 GEMM operands";
+    return cudaErrorInvalidValue;
+  }
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+  gemm_fp8_kernel<<<grid, kGThreads, kGSmem, stream>>>(ta, tb, to, a_scale, b_scale, M, N, K);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_fp8_error(unsigned int *value) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_fp8_error, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_fp8_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ditattn

@@ -29,6 +29,14 @@ cudaError_t launch_layer_norm_modulate(const void *x, const float *scale, const 
 cudaError_t launch_rms_norm(const void *x, const float *w, void *y, long long rows, int C, float eps,
                             cudaStream_t stream);
 
+// W8A8 fp8: per-row dynamic quantisation (K % 8 == 0, K <= quant_fp8_max_k()) and the scaled GEMM.
+int quant_fp8_max_k();
+cudaError_t launch_quant_fp8_rows(const void *x, void *codes, float *scale, long long M, int K, cudaStream_t stream);
+cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,
+                            int M, int N, int K, long long lda, long long ldb, long long ldo, cudaStream_t stream,
+                            const char **detail);
+cudaError_t read_and_clear_fp8_error(unsigned int *value);
+
 // Largest C the merge kernel accepts, and whether C * H weights fit its shared-memory budget.
 int merge_max_parts();
 bool merge_fits(int C, int H);

@@ -20,7 +20,7 @@ DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT 
 DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
-            "dit_layer_norm_modulate", "dit_rms_norm")
+            "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8")
 
 _lib = None
 
@@ -50,10 +50,14 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
                                        i32, vp, vp]
     lib.dit_layer_norm_modulate.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, vp]
     lib.dit_rms_norm.argtypes = [vp, vp, vp, ctypes.c_int64, i32, f32, vp]
+    lib.dit_quant_fp8_rows.argtypes = [vp, vp, vp, ctypes.c_int64, i32, vp]
+    lib.dit_gemm_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                 vp]
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
-                 "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm"):
+                 "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
+                 "dit_quant_fp8_rows", "dit_gemm_fp8"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -197,6 +201,33 @@ def rms_norm(x, w, eps: float = 1e-6, y=None, stream=None):
     _check(lib.dit_rms_norm(x.data_ptr(), w.data_ptr(), y.data_ptr(), x.numel() // C, C, float(eps),
                             _stream(stream)))
     return y
+
+
+def quant_fp8_rows(x, codes=None, scale=None, stream=None):
+    """Per-row dynamic e4m3 quantisation of bf16 x [M, K] -> (codes uint8 [M, K], scale fp32 [M])."""
+    lib = load_library()
+    _cuda(x)
+    M, K = x.shape
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("x must be contiguous bf16 [M, K]")
+    codes = torch.empty((M, K), dtype=torch.uint8, device=x.device) if codes is None else codes
+    scale = torch.empty(M, dtype=torch.float32, device=x.device) if scale is None else scale
+    _check(lib.dit_quant_fp8_rows(x.data_ptr(), codes.data_ptr(), scale.data_ptr(), M, K, _stream(stream)))
+    return codes, scale
+
+
+def gemm_fp8(a, a_scale, b, b_scale, out=None, stream=None):
+    """out[m, n] = a_scale[m] b_scale[n] sum_k A[m, k] B[n, k]; a [M, K], b [N, K] uint8 e4m3 codes -> bf16 [M, N]."""
+    lib = load_library()
+    _cuda(a, b, a_scale, b_scale)
+    M, K = a.shape
+    N = b.shape[0]
+    if a.dtype != torch.uint8 or b.dtype != torch.uint8 or b.shape[1] != K or a.stride(1) != 1 or b.stride(1) != 1:
+        raise ValueError("a, b must be uint8 [M, K] / [N, K] with contiguous rows")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device) if out is None else out
+    _check(lib.dit_gemm_fp8(a.data_ptr(), a_scale.data_ptr(), b.data_ptr(), b_scale.data_ptr(), out.data_ptr(), M, N,
+                            K, a.stride(0), b.stride(0), out.stride(0), _stream(stream)))
+    return out
 
 
 def poll_device_error(stream=None):

@@ -8,6 +8,8 @@
  *                       over all keys or over one key chunk [kv_begin, kv_end)
  *   dit_attn_merge_lse  blockwise log-sum-exp merge of per-chunk (O_c, LSE_c)
  *   dit_attn_fwd_causal the attention with a causal mask (the pages' VLM path)
+ *   dit_layer_norm_modulate, dit_rms_norm   row normalisations of the DiT block
+ *   dit_quant_fp8_rows, dit_gemm_fp8        W8A8 fp8 projection
  *
  * Conventions shared by every entry point
  *   - Tensors are device pointers owned by the caller.  Activations are
@@ -200,6 +202,42 @@ dit_status dit_layer_norm_modulate(const void *x, const float *scale, const floa
  */
 dit_status dit_rms_norm(const void *x, const float *w, void *y, int64_t rows, int C, float eps,
                         struct CUstream_st *stream);
+
+/*
+ * dit_quant_fp8_rows -- per-token dynamic quantisation to fp8 e4m3.
+ *
+ * Defined by: "feat: support Ascend NPU backend (torch_npu) for Qwen-Image
+ * pipelines - #274", item 4 (npu_quant_linear: activations quantised per token
+ * with a dynamic scale before the quantised matmul).
+ *
+ * For every row x of K values: scale = max |x| / 448 (1 for an all-zero row),
+ * code = e4m3(x / scale), rounded to nearest even and saturated to +-448; the
+ * scale and the quotient are fp32.  e4m3 is the OCP 8-bit format with 4
+ * exponent bits (bias 7), 3 mantissa bits and no infinities.
+ *
+ *   x       bf16 [M, K], contiguous, 16-byte aligned
+ *   codes   uint8 [M, K] e4m3 codes, contiguous, 16-byte aligned
+ *   scale   fp32 [M]
+ *   K       a multiple of 16, at most 8192
+ */
+dit_status dit_quant_fp8_rows(const void *x, void *codes, float *scale, int64_t M, int K, struct CUstream_st *stream);
+
+/*
+ * dit_gemm_fp8 -- scaled fp8 GEMM: out[m, n] = a_scale[m] * b_scale[n] * sum_k A[m, k] B[n, k].
+ *
+ * Defined by: the same PR, item 4 (npu_quant_matmul of per-token quantised
+ * activations with per-output-channel quantised weights, output bf16).  A
+ * holds activation codes (row m = token), B weight codes (row n = output
+ * channel); both are e4m3, row-major with K contiguous; accumulation in fp32
+ * on the tensor cores.
+ *
+ *   a, b          uint8 [M, K] / [N, K] with row strides lda / ldb (bytes, multiples of 16)
+ *   a_scale       fp32 [M];  b_scale fp32 [N]
+ *   out           bf16 [M, N] with row stride ldo (elements, multiple of 8)
+ *   K             a positive multiple of 16
+ */
+dit_status dit_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,
+                        int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldo, struct CUstream_st *stream);
 
 /*
  * dit_poll_device_error -- synchronise `stream`, then read and clear the

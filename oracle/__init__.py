@@ -54,6 +54,16 @@ class Oracle:
         lib.oracle_rms_norm.argtypes = [_D, _D, _I64, _I64, ctypes.c_double, _D]
         lib.oracle_layer_norm_modulate.argtypes = [_D, _D, _D, _I64, _I64, _I64, ctypes.c_double, _D]
         lib.oracle_layer_norm_modulate.restype = None
+        _U8 = ctypes.POINTER(ctypes.c_ubyte)
+        _F = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_int]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3_encode.restype = ctypes.c_int
+        lib.oracle_quant_fp8_rows.argtypes = [_D, _I64, _I64, _U8, _F]
+        lib.oracle_quant_fp8_rows.restype = None
+        lib.oracle_gemm_fp8.argtypes = [_U8, _F, _U8, _F, _I64, _I64, _I64, _D]
+        lib.oracle_gemm_fp8.restype = None
         lib.oracle_rope_interleaved.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _D]
         lib.oracle_qk_norm_rope.argtypes = [_D, _D, _D, _D, _I64, _I64, _I64, _I64, ctypes.c_double, _D]
         lib.oracle_attention.argtypes = [_D, _D, _D, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
@@ -90,6 +100,37 @@ class Oracle:
         self.lib.oracle_layer_norm_modulate(_ptr(x), None if sc is None else _ptr(sc), None if sh is None else _ptr(sh),
                                             B, L, C, eps, _ptr(y))
         return y
+
+    def e4m3_decode(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_decode(int(code)))
+
+    def e4m3_encode(self, x: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(x)))
+
+    def quant_fp8_rows(self, x):
+        """x [M, K] -> (codes uint8 [M, K], scale float32 [M]) by per-row absmax / 448."""
+        x = _f64(x)
+        M, K = x.shape
+        codes = np.empty((M, K), dtype=np.uint8)
+        scale = np.empty(M, dtype=np.float32)
+        self.lib.oracle_quant_fp8_rows(_ptr(x), M, K, codes.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)),
+                                       scale.ctypes.data_as(ctypes.POINTER(ctypes.c_float)))
+        return codes, scale
+
+    def gemm_fp8(self, a, a_scale, b, b_scale) -> np.ndarray:
+        """a [M, K], b [N, K] e4m3 codes; a_scale [M], b_scale [N] -> fp64 [M, N]."""
+        a = np.ascontiguousarray(a, dtype=np.uint8)
+        b = np.ascontiguousarray(b, dtype=np.uint8)
+        sa = np.ascontiguousarray(a_scale, dtype=np.float32)
+        sb = np.ascontiguousarray(b_scale, dtype=np.float32)
+        M, K = a.shape
+        N = b.shape[0]
+        out = np.empty((M, N))
+        u8 = ctypes.POINTER(ctypes.c_ubyte)
+        f = ctypes.POINTER(ctypes.c_float)
+        self.lib.oracle_gemm_fp8(a.ctypes.data_as(u8), sa.ctypes.data_as(f), b.ctypes.data_as(u8),
+                                 sb.ctypes.data_as(f), M, N, K, _ptr(out))
+        return out
 
     def rope_interleaved(self, x, cos, sin) -> np.ndarray:
         """x [B, S, H, D]; cos/sin [>=S, D/2]."""

@@ -262,3 +262,81 @@ void oracle_merge_lse(const double *o_parts, const double *lse_parts,
         lse[li] = L;
     }
 }
+
+/*
+ * ---------------------------------------------------------------- W8A8 fp8
+ * "feat: support Ascend NPU backend (torch_npu) for Qwen-Image pipelines -
+ * #274", item 4 (npu_quant_linear): activations are quantised per token
+ * (dynamic, one scale per row), weights per output channel, to fp8 e4m3; the
+ * quantised matmul multiplies the integer-like codes and applies the per-token
+ * and per-channel scales, producing bf16.
+ *
+ * e4m3 (OCP 8-bit floating point, "E4M3"): 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent field 0 holds subnormals m * 2^-9; no
+ * infinities; S.1111.111 is NaN, so the largest finite magnitude is
+ * 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_decode(int code) {
+    const int sgn = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Round x to the nearest e4m3 value (ties to the even code), saturating to +-448. */
+int oracle_e4m3_encode(double x) {
+    int sgn = x < 0 || (x == 0 && signbit(x));
+    double a = fabs(x);
+    if (a >= 448.0) return (sgn << 7) | 0x7E;
+    /* walk the 127 non-negative finite codes: they are ordered by value */
+    int best = 0;
+    double best_err = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double err = fabs(oracle_e4m3_decode(c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (sgn << 7) | best;
+}
+
+/*
+ * Per-token dynamic quantisation of x [M, K]: scale_m = max_k |x_mk| / 448
+ * (1 when the row is all zero), code_mk = e4m3(x_mk / scale_m).  The quotient
+ * x / scale decides the code, so it is formed as the kernel forms it: both
+ * the scale and the quotient rounded to fp32.
+ */
+void oracle_quant_fp8_rows(const double *x, int64_t M, int64_t K, unsigned char *codes, float *scale) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = (float)fabs(x[m * K + k]);
+            if (a > amax) amax = a;
+        }
+        float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[m] = sc;
+        for (int64_t k = 0; k < K; ++k) {
+            float qv = (float)x[m * K + k] / sc;
+            codes[m * K + k] = (unsigned char)oracle_e4m3_encode((double)qv);
+        }
+    }
+}
+
+/* out[m, n] = a_scale[m] * b_scale[n] * sum_k dec(a[m, k]) * dec(b[n, k])  (a [M, K], b [N, K] codes) */
+void oracle_gemm_fp8(const unsigned char *a, const float *a_scale, const unsigned char *b, const float *b_scale,
+                     int64_t M, int64_t N, int64_t K, double *out) {
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = oracle_e4m3_decode(c);
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += lut[a[m * K + k]] * lut[b[n * K + k]];
+            out[m * N + n] = acc * (double)a_scale[m] * (double)b_scale[n];
+        }
+}
+

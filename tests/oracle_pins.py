@@ -334,6 +334,58 @@ def pin_attn_causal_first_row_and_chunks(orc):
     _close(lm, lse, rtol=1e-12, what="causal chunks merged lse")
 
 
+# ---------------------------------------------------------------- fp8 e4m3 (W8A8)
+
+def pin_e4m3_codec(orc):
+    """Spec values, decode/encode round trip of every finite code, and torch's float8_e4m3fn cast."""
+    assert orc.e4m3_decode(0x38) == 1.0 and orc.e4m3_decode(0x7E) == 448.0 and orc.e4m3_decode(0xFE) == -448.0
+    assert orc.e4m3_decode(0x01) == 2.0 ** -9 and orc.e4m3_decode(0x08) == 2.0 ** -6
+    assert math.isnan(orc.e4m3_decode(0x7F))
+    for c in range(256):
+        if c & 0x7F != 0x7F and c != 0x80:
+            assert orc.e4m3_encode(orc.e4m3_decode(c)) == c, hex(c)
+    assert orc.e4m3_encode(1000.0) == 0x7E and orc.e4m3_encode(-1000.0) == 0xFE  # saturating
+    rng = _rng(24)
+    # every midpoint between neighbouring finite codes is a tie: it must go to the even code
+    vals = np.array([orc.e4m3_decode(c) for c in range(0x7F)])
+    mids = (vals[:-1] + vals[1:]) / 2
+    xs = np.concatenate([rng.normal(0, 50, 4000), rng.normal(0, 0.01, 1000), mids, -mids]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([orc.e4m3_encode(float(x)) for x in xs], dtype=np.uint8)
+    assert np.array_equal(ours, ref)
+
+
+def pin_quant_rows(orc):
+    """Per-row scale = absmax / 448; the row's largest magnitude maps to +-448; codes decode near x / scale."""
+    rng = _rng(25)
+    x = rng.normal(0, 3, (6, 40))
+    x[3] = 0.0
+    codes, scale = orc.quant_fp8_rows(x)
+    absmax = np.abs(x.astype(np.float32)).max(axis=1)
+    assert scale[3] == 1.0 and np.all(codes[3] == 0)
+    for m in (0, 1, 2, 4, 5):
+        assert scale[m] == np.float32(absmax[m]) / np.float32(448.0)
+        dec = np.array([orc.e4m3_decode(c) for c in codes[m]])
+        assert np.abs(dec).max() == 448.0
+        q = (x[m].astype(np.float32) / scale[m]).astype(np.float64)
+        assert np.all(np.abs(dec - q) <= np.maximum(np.abs(q) * 2.0 ** -4, 2.0 ** -10))
+
+
+def pin_gemm_fp8(orc):
+    """The scaled fp8 GEMM equals numpy's matmul of the decoded codes times both scales."""
+    rng = _rng(26)
+    a = rng.integers(0, 256, (5, 48)).astype(np.uint8)
+    b = rng.integers(0, 256, (7, 48)).astype(np.uint8)
+    a[a & 0x7F == 0x7F] = 0
+    b[b & 0x7F == 0x7F] = 0
+    sa = rng.uniform(0.1, 2, 5).astype(np.float32)
+    sb = rng.uniform(0.1, 2, 7).astype(np.float32)
+    lut = np.array([orc.e4m3_decode(c) for c in range(256)])
+    lut[np.isnan(lut)] = 0
+    ref = (lut[a] @ lut[b].T) * sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :]
+    _close(orc.gemm_fp8(a, sa, b, sb), ref, rtol=1e-12, atol=1e-12, what="fp8 gemm")
+
+
 # ---------------------------------------------------------------- merge
 
 def _parts(orc, q, k, v, scale, bounds):

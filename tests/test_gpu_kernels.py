@@ -300,3 +300,40 @@ def test_ring_overlap_equals_full_attention(orc):
     ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
     check_o(host_f64(o), ro, what="ring overlap")
     check_lse(host_f64(lse), rl, what="ring overlap")
+
+
+# ---------------------------------------------------------------- W8A8 fp8
+
+@pytest.mark.parametrize("M,K", [(7, 3072), (300, 128), (1, 16), (64, 8192)])
+def test_quant_fp8_rows_bit_exact(orc, M, K):
+    x = inputs.bf16_normal(M * K, seed=M * 13 + K, std=3.0).reshape(M, K)
+    x[0, :] = 0 if M > 1 else x[0, :]
+    codes, scale = ops.quant_fp8_rows(dev_bf16(x))
+    rc, rs = orc.quant_fp8_rows(inputs.bf16_bits_to_f64(x))
+    assert np.array_equal(scale.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 264, 208), (1, 8, 16), (520, 768, 1024)])
+def test_gemm_fp8_parity(orc, M, N, K):
+    xa = inputs.bf16_normal(M * K, seed=M + K, std=2.0).reshape(M, K)
+    xb = inputs.bf16_normal(N * K, seed=N + 3 * K, std=0.05).reshape(N, K)
+    a, sa = ops.quant_fp8_rows(dev_bf16(xa))
+    b, sb = ops.quant_fp8_rows(dev_bf16(xb))
+    out = ops.gemm_fp8(a, sa, b, sb)
+    ref = orc.gemm_fp8(a.cpu().numpy(), sa.cpu().numpy(), b.cpu().numpy(), sb.cpu().numpy())
+    # fp32 accumulation of exact e4m3 products, two fp32 scale multiplies, one bf16 rounding
+    check_bf16_rounding(host_f64(out), ref, "fp8 gemm", atol=1e-5 * np.abs(ref).max())
+
+
+def test_gemm_fp8_strided_output(orc):
+    M, N, K = 130, 72, 64
+    xa = inputs.bf16_normal(M * K, seed=5).reshape(M, K)
+    xb = inputs.bf16_normal(N * K, seed=6).reshape(N, K)
+    a, sa = ops.quant_fp8_rows(dev_bf16(xa))
+    b, sb = ops.quant_fp8_rows(dev_bf16(xb))
+    buf = torch.zeros((M, N + 40), dtype=torch.bfloat16, device="cuda")
+    ops.gemm_fp8(a, sa, b, sb, out=buf[:, :N])
+    ref = orc.gemm_fp8(a.cpu().numpy(), sa.cpu().numpy(), b.cpu().numpy(), sb.cpu().numpy())
+    check_bf16_rounding(host_f64(buf[:, :N]), ref, "fp8 gemm strided", atol=1e-5 * np.abs(ref).max())
+    assert torch.count_nonzero(buf[:, N:]) == 0

@@ -36,6 +36,11 @@ MUTANTS = {
     "ln_unbiased_var": ("const double inv = 1.0 / sqrt(ss / (double)C + eps);",
                         "const double inv = 1.0 / sqrt(ss / (double)(C - 1) + eps);"),
     "ln_scale_not_plus_one": ("yr[c] = (xr[c] - mu) * inv * (1.0 + sc) + sh;", "yr[c] = (xr[c] - mu) * inv * sc + sh;"),
+    "e4m3_bias8": ("else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "e4m3_ties_odd": ("(err == best_err && (c & 1) == 0 && (best & 1) == 1)", "(err == best_err && (c & 1) == 1)"),
+    "quant_scale_127": ("float sc = amax > 0.0f ? amax / 448.0f : 1.0f;", "float sc = amax > 0.0f ? amax / 127.0f : 1.0f;"),
+    "gemm_drops_b_scale": ("out[m * N + n] = acc * (double)a_scale[m] * (double)b_scale[n];",
+                           "out[m * N + n] = acc * (double)a_scale[m];"),
     "merge_weight_vs_max": ("double wgt = exp(lse_parts[c * part_l + li] - L);",
                             "double wgt = exp(lse_parts[c * part_l + li] - mx);"),
     "merge_lse_drops_max": ("double L = mx + log(sum);", "double L = log(sum);"),
