@@ -433,6 +433,45 @@ def run_ring_overlap(args):
                       "attention_tflops_overlapped": w.attention_flops() / res["overlapped"] / 1e9}))
 
 
+def run_qkv_fp8(args):
+    """Diagnostic: per-token e4m3 quantisation of the tokens (B*S x H*D) and the fp8 GEMM with a
+    [3*H*D, H*D] QKV weight, synthetic, timed with CUDA events (L2 flushed before each step)."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import build, ops
+
+    build.build()
+    ops.load_library()
+    w = inputs.WORKLOADS[args.workload]
+    M, K, N = w.B * w.S, w.H * w.D, 3 * w.H * w.D
+    dev = torch.device("cuda")
+    x = torch.from_numpy(inputs.bf16_normal(M * K, seed=7000 + w.index).reshape(M, K)).to(dev).view(torch.bfloat16)
+    wt = torch.from_numpy(inputs.bf16_normal(N * K, seed=7100 + w.index, std=0.02).reshape(N, K)).to(dev)
+    wq, ws = ops.quant_fp8_rows(wt.view(torch.bfloat16))
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    xs = torch.empty(M, dtype=torch.float32, device=dev)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    tq, tg = [], []
+    for i in range(args.warmup + max(args.steps, 5)):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        ops.quant_fp8_rows(x, xq, xs)
+        e[1].record()
+        ops.gemm_fp8(xq, xs, wq, ws, out=out)
+        e[2].record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            tq.append(e[0].elapsed_time(e[1]))
+            tg.append(e[1].elapsed_time(e[2]))
+    ops.poll_device_error()
+    t_q, t_g = statistics.median(tq), statistics.median(tg)
+    print(json.dumps({"mode": "qkv_fp8", "workload": w.name, "M": M, "N": N, "K": K,
+                      "quant_ms": t_q, "quant_GBps": 3 * M * K / t_q / 1e6,
+                      "gemm_ms": t_g, "gemm_TFLOPs": 2 * M * N * K / t_g / 1e9}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -446,6 +485,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ring-overlap", type=int, default=0, metavar="RANKS",
                     help="time the one-GPU ring-overlap emulation with RANKS key shards instead (diagnostic)")
+    ap.add_argument("--qkv-fp8", action="store_true",
+                    help="time the W8A8 fp8 QKV projection of the workload's tokens instead (diagnostic)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -457,6 +498,8 @@ def main():
         run_reference(args)
     elif args.ring_overlap:
         run_ring_overlap(args)
+    elif args.qkv_fp8:
+        run_qkv_fp8(args)
     else:
         run_ours(args)
 
