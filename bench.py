@@ -37,6 +37,11 @@ FALLBACK_TFLOPS = 1900.0
 FALLBACK_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480": "f32", "wan720": "bf16"}
+# How the KV chunks are combined: "update" folds each later chunk into the running (O, LSE) in its attention
+# epilogue; "kernel" writes stacked per-chunk partials and runs the LSE-merge kernel (Wan720's workload
+# specifies per-chunk bf16 partials merged by the merge kernel).
+MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", "wan480": "kernel",
+         "wan720": "kernel"}
 # DRAM bytes per attention launch (read + write) from an ncu capture of the bench step
 # (profiles/launch_list_qwen_image_step.md), valid for the attention source it was taken on.
 ATTN_TRAFFIC = {"source_sha256_prefix": "9fcb952b8c9608e4", "qwen_image": (39.3 + 56.2) * 1e6}
@@ -187,9 +192,16 @@ def run_reference(args):
     }))
 
 
+def merge_mode(w, args):
+    return args.merge if args.merge != "auto" else MERGE[w.name]
+
+
 def config_of(w, chunks, args):
     return {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "D": w.D, "Sq": w.S, "Skv": w.S,
-            "kv_chunks": chunks, "partial_o": PARTIAL[w.name], "prologue": w.prologue, "causal": False,
+            "kv_chunks": chunks, "partial_o": PARTIAL[w.name],
+            "merge": (merge_mode(w, args) + (" (fused in the last chunk's epilogue)" if merge_mode(w, args) == "update"
+                                             else " (LSE-merge kernel)")) if chunks > 1 else "none",
+            "prologue": w.prologue, "causal": False,
             "scale": "1/sqrt(D)", "l2": "flushed before every timed step (512 MiB write)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
@@ -260,7 +272,8 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    launches_per_step = (1 if w.prologue else 0) + chunks + (1 if chunks > 1 else 0)
+    merge = merge_mode(w, args)
+    launches_per_step = (1 if w.prologue else 0) + chunks + (1 if chunks > 1 and merge == "kernel" else 0)
 
     def step(attn_events=None):
         if w.prologue:
@@ -277,6 +290,16 @@ def run_ours(args):
             return
         if attn_events is not None:
             attn_events[0].record(stream)
+        if merge == "update":
+            # chunk 0 starts the running result; later chunks merge into it in their epilogues, the last one
+            # straight into the bf16 output
+            ops.attn_fwd(aq, ak, v, None, *bounds[0], o=o_parts[0], lse=lse)
+            for lo, hi in bounds[1:-1]:
+                ops.attn_fwd_update(aq, ak, v, o_parts[0], lse, None, lo, hi, o=o_parts[0], lse=lse)
+            ops.attn_fwd_update(aq, ak, v, o_parts[0], lse, None, *bounds[-1], o=o, lse=lse)
+            if attn_events is not None:
+                attn_events[1].record(stream)
+            return
         for c, (lo, hi) in enumerate(bounds):
             ops.attn_fwd(aq, ak, v, None, lo, hi, o=o_parts[c], lse=lse_parts[c])
         if attn_events is not None:
@@ -341,7 +364,8 @@ def run_ours(args):
         for src, dst in zip(pin_small, dsmall):
             dst.copy_(src, non_blocking=True)
         oo, ll = ops.dit_attention(dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16),
-                                   *dsmall, eps=w.eps, chunks=chunks, partial_dtype=pdt, prologue=w.prologue)
+                                   *dsmall, eps=w.eps, chunks=chunks, partial_dtype=pdt, prologue=w.prologue,
+                                   merge=merge)
         o_host.copy_(oo, non_blocking=True)
         lse_host.copy_(ll, non_blocking=True)
 
@@ -480,6 +504,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--chunks", type=int, default=0, help="KV chunks (0: the workload's own)")
+    ap.add_argument("--merge", choices=["auto", "kernel", "update"], default="auto",
+                    help="combine KV chunks by the merge kernel or in the attention epilogue (auto: the workload's)")
     ap.add_argument("--ref-rows", type=int, default=48, help="query rows per (b, h) in each reference step")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

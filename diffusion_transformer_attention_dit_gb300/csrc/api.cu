@@ -81,10 +81,15 @@ dit_status dit_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_o
 
 namespace {
 
+// o_acc == nullptr: plain form.  Otherwise the update form, whose running result
+// (o_acc, lse_acc) may be the output itself (same pointer, dtype and strides) or
+// must not overlap any other argument.
 dit_status attn_common(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                        const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin, int kv_end,
                        bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
-                       struct CUstream_st *stream) {
+                       struct CUstream_st *stream, bool update = false, const void *o_acc = nullptr,
+                       dit_dtype acc_dtype = DIT_BF16, const int64_t acc_strides[3] = nullptr,
+                       const float *lse_acc = nullptr) {
   g_detail = "";
   if (B < 0 || H < 0 || Sq < 0 || Skv < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
   if (D != 64 && D != 128) return fail(DIT_ERR_UNSUPPORTED, "head dim must be 64 or 128");
@@ -95,6 +100,11 @@ dit_status attn_common(const void *q, const void *k, const void *v, int B, int H
   if (kv_begin < 0 || kv_begin >= kv_end || kv_end > Skv)
     return fail(DIT_ERR_INVALID_ARG, "key range must satisfy 0 <= kv_begin < kv_end <= Skv");
   if (!q || !k || !v || !o || !lse) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+  if (update) {
+    if (!o_acc || !lse_acc) return fail(DIT_ERR_INVALID_ARG, "null pointer");
+    if (!acc_strides) return fail(DIT_ERR_INVALID_ARG, "null stride array");
+    if (acc_dtype != DIT_BF16 && acc_dtype != DIT_F32) return fail(DIT_ERR_INVALID_ARG, "unknown running-output dtype");
+  }
   const int osz = o_dtype == DIT_F32 ? 4 : 2;
   for (int i = 0; i < 3; ++i) {
     if (q_strides[i] <= 0 || kv_strides[i] <= 0 || o_strides[i] <= 0)
@@ -113,9 +123,26 @@ dit_status attn_common(const void *q, const void *k, const void *v, int B, int H
   if (overlap(ro, rq) || overlap(ro, rk) || overlap(ro, rv) || overlap(rl, rq) || overlap(rl, rk) ||
       overlap(rl, rv) || overlap(rl, ro))
     return fail(DIT_ERR_INVALID_ARG, "outputs overlap inputs or each other");
+  if (update) {
+    const int asz = acc_dtype == DIT_F32 ? 4 : 2;
+    for (int i = 0; i < 3; ++i) {
+      if (acc_strides[i] <= 0) return fail(DIT_ERR_INVALID_ARG, "strides must be positive");
+      if ((acc_strides[i] * asz) % 16) return fail(DIT_ERR_INVALID_ARG, "byte strides must be multiples of 16");
+    }
+    if (!aligned(o_acc, 16) || !aligned(lse_acc, 4)) return fail(DIT_ERR_INVALID_ARG, "pointer misaligned");
+    const Range ra = bshd_range(o_acc, B, Sq, H, D, acc_strides, asz);
+    const Range rla = {reinterpret_cast<uintptr_t>(lse_acc),
+                       reinterpret_cast<uintptr_t>(lse_acc) + (uintptr_t)B * H * Sq * 4};
+    const bool acc_in_place = o_acc == o && acc_dtype == o_dtype && acc_strides[0] == o_strides[0] &&
+                              acc_strides[1] == o_strides[1] && acc_strides[2] == o_strides[2];
+    if ((!acc_in_place && overlap(ra, ro)) || overlap(ra, rl) || (lse_acc != lse && overlap(rla, rl)) ||
+        overlap(rla, ro))
+      return fail(DIT_ERR_INVALID_ARG, "running result overlaps an output (only exact in-place is allowed)");
+  }
   const char *detail = nullptr;
   cudaError_t e = ditattn::launch_attn_fwd(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end,
-                                           causal, o, o_dtype == DIT_F32, o_strides, lse,
+                                           causal, o, o_dtype == DIT_F32, o_strides, lse, update ? o_acc : nullptr,
+                                           acc_dtype == DIT_F32, acc_strides, lse_acc,
                                            reinterpret_cast<cudaStream_t>(stream), &detail);
   return from_cuda(e, detail);
 }
@@ -138,6 +165,16 @@ dit_status dit_attn_fwd_causal(const void *q, const void *k, const void *v, int 
                                struct CUstream_st *stream) {
   return attn_common(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end, true, o, o_dtype,
                      o_strides, lse, stream);
+}
+
+dit_status dit_attn_fwd_update(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                               const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
+                               int kv_end, int causal, const void *o_acc, dit_dtype acc_dtype,
+                               const int64_t acc_strides[3], const float *lse_acc, void *o, dit_dtype o_dtype,
+                               const int64_t o_strides[3], float *lse, struct CUstream_st *stream) {
+  if (causal != 0 && causal != 1) return fail(DIT_ERR_INVALID_ARG, "causal must be 0 or 1");
+  return attn_common(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end, causal == 1, o,
+                     o_dtype, o_strides, lse, stream, true, o_acc, acc_dtype, acc_strides, lse_acc);
 }
 
 dit_status dit_attn_merge_lse(const void *o_parts, dit_dtype in_dtype, const float *lse_parts, int C, int B, int H,

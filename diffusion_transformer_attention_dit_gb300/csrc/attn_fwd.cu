@@ -25,6 +25,12 @@
 //               the idle Q buffer in swizzled layout and written by TMA;
 //               LSE = (m + log2 l) ln 2.
 // TMEM (512 columns): S/P of tile 0 | S/P of tile 1 | O of tile 0 | O of tile 1.
+//
+// Update form (same PR, item 2: update_out_and_lse after each ring step): with a
+// running result (O_acc, LSE_acc) of earlier key ranges, the epilogue writes
+//   L = ln(e^LSE_acc + e^LSE_c),  O = e^(LSE_acc - L) O_acc + e^(LSE_c - L) O_c
+// so the block's own O never reaches memory.  The O_acc tiles are loaded by TMA
+// into K/V ring slots freed by the last blocks, as further fills of the ring.
 // Every mbarrier wait is bounded (about 2 s); a wait that gives up sets the
 // library's device error word and the CTA drains its in-flight copies and MMAs,
 // frees TMEM and exits.
@@ -81,6 +87,8 @@ struct AttnArgs {
   long long o_sb, o_ss, o_sh;
   int o_f32;
   float *lse;
+  const float *lse_acc;  // update form: running LSE [B, H, Sq] (may equal lse)
+  int acc_f32;           // update form: O_acc is fp32 (else bf16)
 };
 
 // Bounded wait; false (and the device error word set) if the phase did not complete in time.
@@ -140,11 +148,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int D, bool kCausal>
+template <int D, bool kCausal, bool kUpdate>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                    const AttnArgs args) {
+                    const __grid_constant__ CUtensorMap tm_acc, const AttnArgs args) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -161,6 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int reach = q_last - args.kv_begin + 1;  // keys of the range visible to the last row
     nblk = max(1, min(nblk, (reach + kBN - 1) / kBN));
   }
+  // Update form: the O_acc tile of query tile t, half hf, is ring fill 2 * nblk + hf * kNQ + t
+  // (one 128 x D bf16 tile, or two halves of an fp32 tile, per ring slot).
+  const int acc_halves = kUpdate ? (args.acc_f32 ? 2 : 1) : 0;
 
   const uint32_t bars = base + L::kBar;
   const uint32_t q_full = bars;
@@ -190,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tm_k);
     tma_prefetch_map(&tm_v);
     tma_prefetch_map(&tm_o);
+    if (kUpdate) tma_prefetch_map(&tm_acc);
   }
   if (warp == kWarpMma) {
     tmem_alloc(base + L::kTmemSlot, kTmemCols);
@@ -222,6 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(dst + hf * L::kBox, which ? &tm_v : &tm_k, slot_full(slot), hf * 64, h, j * kBN, b);
           ++issued;
         }
+      }
+      // Update form: the O_acc tiles follow the last K/V block through the ring.
+      // A slot holds D / 64 boxes of 128 rows x 128 bytes: a whole bf16 tile, or
+      // half of an fp32 tile (boxes of 32 columns).
+      for (int p = 0; p < acc_halves * kNQ && ok; ++p) {
+        const int i = 2 * nblk + p, slot = i % kSlots, t = p % kNQ, hf = p / kNQ;
+        if (!wait_bounded(slot_empty(slot), ((i / kSlots) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(slot_full(slot), L::kTile);
+        const uint32_t dst = base + L::kKV + slot * L::kTile;
+        const int cols = args.acc_f32 ? 32 : 64;  // columns per box
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_4d(dst + bx * L::kBox, &tm_acc, slot_full(slot), (hf * (D / 64) + bx) * cols, h,
+                      q0 + t * kBM, b);
+        ++issued;
       }
       // Every copy issued must land before the CTA may exit.
       wait_bounded(q_full, 0);
@@ -377,6 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(p_full(t));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_done(t), 0));
+    if (kUpdate && ok) {  // this tile's O_acc halves have landed
+      bool got = true;
+      for (int hf = 0; hf < acc_halves; ++hf) {
+        const int i = 2 * nblk + hf * kNQ + t;
+        got = got && wait_bounded(slot_full(i % kSlots), (i / kSlots) & 1);
+      }
+      ok = __all_sync(0xffffffffu, got);
+    }
     // Every warp of the warpgroup gets here (all waits above are bounded); the
     // epilogue's named barriers run only if all four warps are on the normal path.
     ok = named_barrier_and(1 + t, 128, ok);
@@ -386,8 +423,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // map, then stored by TMA as whole 128-byte rows.  fp32 output is twice the
       // buffer, so it goes in two rounds.
       tc_fence_after_sync();
-      const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row with no visible key outputs zeros
-      const uint64_t il2 = f2(inv_l, inv_l);
+      const int tile_q0 = q0 + t * kBM;
+      // Output row = wc * (unnormalised O in TMEM) + wa * O_acc row.  Plain form:
+      // wc = 1 / l, wa = 0 (a row with no visible key outputs zeros).
+      float wc = l > 0.f ? 1.0f / l : 0.f, wa = 0.f;
+      float lse_out = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (kUpdate) {
+        // base 2: this range's LSE is m + log2 l; O_c = acc / l, so its weight
+        // e^(LSE_c - L) / l is 2^(m - L2)
+        const int q = tile_q0 + row;
+        const float la = q < args.Sq ? args.lse_acc[((long long)b * args.H + h) * args.Sq + q] * 1.4426950408889634f
+                                     : -INFINITY;
+        const float lc = l > 0.f ? m + log2f(l) : -INFINITY;
+        const float mx = fmaxf(la, lc);
+        if (mx == -INFINITY) {  // neither part has seen a key: O = 0, LSE = -inf
+          wa = 0.f;
+          wc = 0.f;
+          lse_out = -INFINITY;
+        } else {
+          const float L2 = mx + log2f(ex2(la - mx) + ex2(lc - mx));
+          wa = ex2(la - L2);
+          wc = l > 0.f ? ex2(m - L2) : 0.f;
+          lse_out = L2 * 0.69314718055994531f;
+        }
+      }
+      const uint64_t wc2 = f2(wc, wc), wa2 = f2(wa, wa);
       const uint32_t stage = base + L::kQ + t * L::kTile;
       const bool f32 = args.o_f32 != 0;
       const int W = f32 ? 32 : 64;          // output columns per 128-byte box row
@@ -395,7 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kPerRound = D / 64;     // boxes that fit in the staging buffer
       const uint32_t row_addr = stage + row * 128;
       const uint32_t sw = row & 7;          // 128-byte swizzle: chunk index XOR row % 8
-      const int tile_q0 = q0 + t * kBM;
       for (int r0 = 0; r0 < n_boxes; r0 += kPerRound) {
         if (r0 > 0) {  // the previous round's boxes must have been read before reuse
           if (row == 0) bulk_wait_read_all();
@@ -404,6 +463,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = r0 * W / 32; c < (r0 + kPerRound) * W / 32; ++c) {
           uint32_t o[32];
           tmem_ld_x32(tO + c * 32, o);
+          if (kUpdate) {
+            // the same 32 columns of this row of O_acc, from its ring slot
+            float a[32];
+            if (args.acc_f32) {  // box c of the tile, in half c / (D / 64)
+              const int i = 2 * nblk + (c / (D / 64)) * kNQ + t;
+              const uint32_t src = base + L::kKV + (i % kSlots) * L::kTile + (c % (D / 64)) * L::kBox + row * 128;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                uint32_t x0, x1, x2, x3;
+                ld_shared_v4(src + ((u ^ sw) << 4), x0, x1, x2, x3);
+                a[4 * u] = __uint_as_float(x0), a[4 * u + 1] = __uint_as_float(x1);
+                a[4 * u + 2] = __uint_as_float(x2), a[4 * u + 3] = __uint_as_float(x3);
+              }
+            } else {  // box c / 2 (64 bf16 columns), 16-byte chunks 4 * (c % 2) ..
+              const int i = 2 * nblk + t;
+              const uint32_t src = base + L::kKV + (i % kSlots) * L::kTile + (c / 2) * L::kBox + row * 128;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint32_t x[4];
+                ld_shared_v4(src + (((4 * (c & 1) + u) ^ sw) << 4), x[0], x[1], x[2], x[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  a[8 * u + 2 * e] = __uint_as_float(x[e] << 16);
+                  a[8 * u + 2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float y0, y1;
+              f2_split(f2_fma(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), wc2,
+                              f2_mul(f2(a[2 * i], a[2 * i + 1]), wa2)),
+                       y0, y1);
+              o[2 * i] = __float_as_uint(y0), o[2 * i + 1] = __float_as_uint(y1);
+            }
+          }
+          const uint64_t il2 = kUpdate ? f2(1.f, 1.f) : wc2;
           const int col0 = c * 32;
           const uint32_t dst = row_addr + (col0 / W - r0) * L::kBox;
           const int chunk0 = (col0 % W) / (f32 ? 4 : 8);
@@ -441,8 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (row == 0) bulk_wait_read_all();
       const int q = tile_q0 + row;
-      if (q < args.Sq)
-        args.lse[((long long)b * args.H + h) * args.Sq + q] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (q < args.Sq) args.lse[((long long)b * args.H + h) * args.Sq + q] = lse_out;
     }
   }
 
@@ -496,9 +591,9 @@ bool encode_bshd(CUtensorMap *map, const void *ptr, int B, int S, int H, int D, 
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool kCausal>
+template <int D, bool kCausal, bool kUpdate>
 cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &to,
-                         const AttnArgs &a, int B, cudaStream_t stream) {
+                         const CUtensorMap &tacc, const AttnArgs &a, int B, cudaStream_t stream) {
   using Lay = Layout<D>;
   static_assert(Lay::kAlloc <= 232448, "shared memory budget");
   int dev = 0;
@@ -506,12 +601,13 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   if (e != cudaSuccess) return e;
   static bool configured[64] = {};
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kCausal>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kCausal, kUpdate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   dim3 grid((a.Sq + kBM * kNQ - 1) / (kBM * kNQ), a.H, B);
-  attn_fwd_kernel<D, kCausal><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, to, a);
+  attn_fwd_kernel<D, kCausal, kUpdate><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, to, tacc, a);
   return cudaGetLastError();
 }
 
@@ -519,10 +615,11 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 
 cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                             const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
-                            bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
+                            bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
+                            bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
                             const char **detail) {
   (void)Skv;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv, to, tacc;
   const int n_kv = kv_end - kv_begin;
   const char *k0 = static_cast<const char *>(k) + (int64_t)kv_begin * kv_st[1] * 2;
   const char *v0 = static_cast<const char *>(v) + (int64_t)kv_begin * kv_st[1] * 2;
@@ -531,6 +628,12 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
     *detail = "cuTensorMapEncodeTiled failed (driver entry point missing or strides/extents unsupported)";
     return cudaErrorInvalidValue;
   }
+  const bool update = o_acc != nullptr;
+  if (update && !encode_bshd(&tacc, o_acc, B, Sq, H, D, acc_st, acc_f32)) {
+    *detail = "cuTensorMapEncodeTiled failed for the running output";
+    return cudaErrorInvalidValue;
+  }
+  if (!update) tacc = to;
   AttnArgs a;
   a.H = H;
   a.Sq = Sq;
@@ -543,11 +646,20 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   a.o_sh = o_st[2];
   a.o_f32 = o_f32 ? 1 : 0;
   a.lse = lse;
+  a.lse_acc = lse_acc;
+  a.acc_f32 = acc_f32 ? 1 : 0;
+  if (update) {
+    if (causal)
+      return D == 64 ? launch_typed<64, true, true>(tq, tk, tv, to, tacc, a, B, stream)
+                     : launch_typed<128, true, true>(tq, tk, tv, to, tacc, a, B, stream);
+    return D == 64 ? launch_typed<64, false, true>(tq, tk, tv, to, tacc, a, B, stream)
+                   : launch_typed<128, false, true>(tq, tk, tv, to, tacc, a, B, stream);
+  }
   if (causal)
-    return D == 64 ? launch_typed<64, true>(tq, tk, tv, to, a, B, stream)
-                   : launch_typed<128, true>(tq, tk, tv, to, a, B, stream);
-  return D == 64 ? launch_typed<64, false>(tq, tk, tv, to, a, B, stream)
-                 : launch_typed<128, false>(tq, tk, tv, to, a, B, stream);
+    return D == 64 ? launch_typed<64, true, false>(tq, tk, tv, to, tacc, a, B, stream)
+                   : launch_typed<128, true, false>(tq, tk, tv, to, tacc, a, B, stream);
+  return D == 64 ? launch_typed<64, false, false>(tq, tk, tv, to, tacc, a, B, stream)
+                 : launch_typed<128, false, false>(tq, tk, tv, to, tacc, a, B, stream);
 }
 
 cudaError_t launch_wait_timeout_selftest(cudaStream_t stream) {

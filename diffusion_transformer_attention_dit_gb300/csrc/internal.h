@@ -8,10 +8,12 @@
 namespace ditattn {
 
 // Attention forward over keys [kv_begin, kv_end) (causal: query i sees keys j <= i).
-// Strides in elements {b, s, h}.
+// Strides in elements {b, s, h}.  With o_acc non-null (update form) the result is
+// LSE-merged with the running (o_acc, lse_acc) before it is written.
 cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                             const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
-                            bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, cudaStream_t stream,
+                            bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
+                            bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
                             const char **detail);
 
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,

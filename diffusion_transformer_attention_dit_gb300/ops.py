@@ -20,7 +20,7 @@ DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT 
 DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
-            "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8")
+            "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update")
 
 _lib = None
 
@@ -46,6 +46,8 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i64p, i64p, f32, i32, i32, vp, i32, i64p,
                                  vp, vp]
     lib.dit_attn_fwd_causal.argtypes = lib.dit_attn_fwd.argtypes
+    lib.dit_attn_fwd_update.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i64p, i64p, f32, i32, i32, i32, vp, i32,
+                                        i64p, vp, vp, i32, i64p, vp, vp]
     lib.dit_attn_merge_lse.argtypes = [vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_int64, ctypes.c_int64, vp,
                                        i32, vp, vp]
     lib.dit_layer_norm_modulate.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, vp]
@@ -57,7 +59,7 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_selftest_wait_timeout.argtypes = [vp]
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
-                 "dit_quant_fp8_rows", "dit_gemm_fp8"):
+                 "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -151,6 +153,39 @@ def attn_fwd(q, k, v, scale: float | None = None, kv_begin: int = 0, kv_end: int
     return o, lse
 
 
+def attn_fwd_update(q, k, v, o_acc, lse_acc, scale: float | None = None, kv_begin: int = 0, kv_end: int | None = None,
+                    o=None, lse=None, o_dtype=torch.bfloat16, stream=None, causal: bool = False):
+    """Attention over keys [kv_begin, kv_end) LSE-merged into the running result (o_acc, lse_acc) of earlier key
+    ranges, in the attention's epilogue.  o / lse may be o_acc / lse_acc (in place).  Returns (o, lse)."""
+    lib = load_library()
+    _cuda(q, k, v, o_acc, lse_acc)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[2] != H or k.shape[3] != D:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k, v must be bf16")
+    if k.stride() != v.stride():
+        raise ValueError("k and v must share strides")
+    if tuple(o_acc.shape) != (B, Sq, H, D):
+        raise ValueError("o_acc must be [B, Sq, H, D]")
+    for t in (lse_acc, lse):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (B, H, Sq)):
+            raise ValueError("lse and lse_acc must be contiguous fp32 [B, H, Sq]")
+    kv_end = Skv if kv_end is None else kv_end
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if o is None:
+        o = torch.empty((B, Sq, H, D), dtype=o_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    _check(lib.dit_attn_fwd_update(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, H, Sq, Skv, D, _bshd_strides(q),
+                                   _bshd_strides(k), float(scale), int(kv_begin), int(kv_end), int(bool(causal)),
+                                   o_acc.data_ptr(), _dtype_code(o_acc.dtype), _bshd_strides(o_acc),
+                                   lse_acc.data_ptr(), o.data_ptr(), _dtype_code(o.dtype), _bshd_strides(o),
+                                   lse.data_ptr(), _stream(stream)))
+    return o, lse
+
+
 def attn_merge_lse(o_parts, lse_parts, out_dtype=torch.bfloat16, o=None, lse=None, stream=None):
     """Merge C partials: o_parts [C, B, Sq, H, D] (bf16/fp32), lse_parts fp32 [C, B, H, Sq]."""
     lib = load_library()
@@ -241,17 +276,30 @@ def selftest_wait_timeout(stream=None):
 
 
 def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1, scale: float | None = None,
-                  partial_dtype=torch.float32, out_dtype=torch.bfloat16, prologue: bool = True, stream=None):
-    """The whole hot path: prologue, attention over `chunks` KV chunks, LSE merge.  Returns (o, lse)."""
+                  partial_dtype=torch.float32, out_dtype=torch.bfloat16, prologue: bool = True, stream=None,
+                  merge: str = "kernel"):
+    """The whole hot path: prologue, attention over `chunks` KV chunks, LSE merge.  Returns (o, lse).
+
+    merge="kernel": every chunk writes (O_c, LSE_c) into stacked partials and one merge kernel combines them.
+    merge="update": chunk 0 writes a running result (partial_dtype), every later chunk is LSE-merged into it in
+    its attention epilogue, the last one straight into the output."""
     B, S, H, D = q.shape
     Skv = k.shape[1]
     if prologue:
         q, k = qk_norm_rope(q, k, wq, wk, cos, sin, eps, stream=stream)
     if chunks == 1:
         return attn_fwd(q, k, v, scale, o_dtype=out_dtype, stream=stream)
+    edges = [(i * Skv) // chunks for i in range(chunks + 1)]
+    if merge == "update":
+        acc, lse = attn_fwd(q, k, v, scale, edges[0], edges[1], o_dtype=partial_dtype, stream=stream)
+        for c in range(1, chunks - 1):
+            attn_fwd_update(q, k, v, acc, lse, scale, edges[c], edges[c + 1], o=acc, lse=lse, stream=stream)
+        o = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
+        return attn_fwd_update(q, k, v, acc, lse, scale, edges[-2], edges[-1], o=o, lse=lse, stream=stream)
+    if merge != "kernel":
+        raise ValueError("merge must be 'kernel' or 'update'")
     o_parts = torch.empty((chunks, B, S, H, D), dtype=partial_dtype, device=q.device)
     lse_parts = torch.empty((chunks, B, H, S), dtype=torch.float32, device=q.device)
-    edges = [(i * Skv) // chunks for i in range(chunks + 1)]
     for c in range(chunks):
         attn_fwd(q, k, v, scale, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c], stream=stream)
     return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype, stream=stream)

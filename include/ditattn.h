@@ -8,6 +8,8 @@
  *                       over all keys or over one key chunk [kv_begin, kv_end)
  *   dit_attn_merge_lse  blockwise log-sum-exp merge of per-chunk (O_c, LSE_c)
  *   dit_attn_fwd_causal the attention with a causal mask (the pages' VLM path)
+ *   dit_attn_fwd_update the attention of one key range LSE-merged into a running
+ *                       result in its epilogue (the ring step's update_out_and_lse)
  *   dit_layer_norm_modulate, dit_rms_norm   row normalisations of the DiT block
  *   dit_quant_fp8_rows, dit_gemm_fp8        W8A8 fp8 projection
  *
@@ -135,6 +137,42 @@ dit_status dit_attn_fwd_causal(const void *q, const void *k, const void *v,
                                int B, int H, int Sq, int Skv, int D,
                                const int64_t q_strides[3], const int64_t kv_strides[3],
                                float scale, int kv_begin, int kv_end,
+                               void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                               struct CUstream_st *stream);
+
+/*
+ * dit_attn_fwd_update -- attention over one key range, merged into a running result.
+ *
+ * (o_acc, lse_acc) is the result of attention over earlier, disjoint key ranges
+ * (any earlier dit_attn_fwd / dit_attn_fwd_update output).  This call computes
+ * (O_c, LSE_c) over keys [kv_begin, kv_end) exactly as dit_attn_fwd (causal = 1:
+ * as dit_attn_fwd_causal) and writes, per (b, h, i),
+ *   L = ln(exp(lse_acc) + exp(LSE_c))
+ *   o = exp(lse_acc - L) * o_acc + exp(LSE_c - L) * O_c,   lse = L
+ * (both -inf: o = 0, lse = -inf).  O_c itself is never written: the merge runs
+ * in the attention's epilogue, with the o_acc tile brought into shared memory
+ * by the tensor-memory accelerator.
+ *
+ * Defined by: "feat: support Ascend NPU backend (torch_npu) for Qwen-Image
+ * pipelines - #274", item 2 (ring attention: after each KV block the block's
+ * output and LSE are folded into the running ones by update_out_and_lse), and
+ * the Wan2.2 page, section "Ring Attention Overlap" (two attentions combined by
+ * their LSEs).
+ *
+ *   o_acc        [B, Sq, H, D] of acc_dtype (bf16 or fp32), element strides acc_strides
+ *   lse_acc      fp32 [B, H, Sq], contiguous, 4-byte aligned
+ *   o, lse       as for dit_attn_fwd
+ *   causal       0 or 1
+ * In place is allowed: o == o_acc with the same dtype and strides, and/or
+ * lse == lse_acc.  Otherwise the running result must not overlap o or lse.
+ * Other arguments, layouts and errors as for dit_attn_fwd.
+ */
+dit_status dit_attn_fwd_update(const void *q, const void *k, const void *v,
+                               int B, int H, int Sq, int Skv, int D,
+                               const int64_t q_strides[3], const int64_t kv_strides[3],
+                               float scale, int kv_begin, int kv_end, int causal,
+                               const void *o_acc, dit_dtype acc_dtype, const int64_t acc_strides[3],
+                               const float *lse_acc,
                                void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
                                struct CUstream_st *stream);
 

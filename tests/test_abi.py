@@ -84,6 +84,42 @@ def test_attn_empty_work_is_ok_without_launch(lib):
     assert _attn(lib, Sq=0) == ops.DIT_OK
 
 
+def _update(lib, **kw):
+    a = dict(q=A16, k=A16 * 2, v=A16 * 3, B=1, H=2, Sq=256, Skv=256, D=128, qs=_st(256 * 256, 256, 128),
+             kvs=_st(256 * 256, 256, 128), scale=0.088, lo=0, hi=256, causal=0, acc=A16 * 32, ad=1,
+             acs=_st(256 * 256, 256, 128), lacc=A16 * 48, o=A16 * 8, od=0, os=_st(256 * 256, 256, 128),
+             lse=A16 * 16)
+    a.update(kw)
+    return lib.dit_attn_fwd_update(a["q"], a["k"], a["v"], a["B"], a["H"], a["Sq"], a["Skv"], a["D"], a["qs"],
+                                   a["kvs"], a["scale"], a["lo"], a["hi"], a["causal"], a["acc"], a["ad"], a["acs"],
+                                   a["lacc"], a["o"], a["od"], a["os"], a["lse"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(causal=2), ops.DIT_ERR_INVALID_ARG),
+    (dict(acc=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(lacc=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(acs=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(ad=7), ops.DIT_ERR_INVALID_ARG),
+    (dict(acc=A16 * 32 + 8), ops.DIT_ERR_INVALID_ARG),          # misaligned
+    (dict(acs=_st(256 * 256, 254, 128)), ops.DIT_ERR_INVALID_ARG),  # fp32 stride not a multiple of 16 bytes
+    (dict(acc=A16 * 8 + 256), ops.DIT_ERR_INVALID_ARG),         # overlaps o without being it
+    (dict(acc=A16 * 8), ops.DIT_ERR_INVALID_ARG),               # same pointer as o but another dtype
+    (dict(lacc=A16 * 8 + 64), ops.DIT_ERR_INVALID_ARG),         # running LSE inside o
+    (dict(lacc=A16 * 16 + 4), ops.DIT_ERR_INVALID_ARG),         # running LSE overlaps lse without being it
+    (dict(lo=5, hi=5), ops.DIT_ERR_INVALID_ARG),
+    (dict(D=96), ops.DIT_ERR_UNSUPPORTED),
+])
+def test_update_rejects_bad_arguments(lib, kw, code):
+    assert _update(lib, **kw) == code
+    assert lib.dit_last_error_detail() != b""
+
+
+def test_update_empty_work_is_ok_without_launch(lib):
+    assert _update(lib, Sq=0) == ops.DIT_OK
+    assert _update(lib, B=0, acc=None) == ops.DIT_OK
+
+
 def _prologue(lib, **kw):
     a = dict(q=A16, k=A16 * 2, qo=A16 * 3, ko=A16 * 4, wq=A16 * 5, wk=A16 * 6, cos=A16 * 7, sin=A16 * 8, B=1, S=16,
              H=2, D=128, eps=1e-6)

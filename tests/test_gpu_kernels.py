@@ -175,6 +175,98 @@ def test_chunked_merged_equals_full(orc, C, partial):
         assert (host_f64(om) - host_f64(o_parts[c])).__abs__().max() > 0.05
 
 
+# ---------------------------------------------------------------- update form (merge in the epilogue)
+
+UPDATE_SHAPES = [
+    # B, H, Sq, Skv, D, split
+    (1, 2, 256, 256, 128, 128),
+    (2, 3, 200, 333, 128, 129),
+    (1, 2, 517, 300, 64, 37),
+    (1, 1, 1, 2, 128, 1),
+    (2, 2, 300, 700, 64, 650),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,D,split", UPDATE_SHAPES)
+@pytest.mark.parametrize("acc_dt,out_dt", [("f32", "bf16"), ("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
+def test_attn_update_parity(orc, B, H, Sq, Skv, D, split, acc_dt, out_dt):
+    """Chunk [0, split) as the running result, then [split, Skv) merged into it in the epilogue == full attention."""
+    dts = {"bf16": torch.bfloat16, "f32": torch.float32}
+    q, k, v, *_ = inputs.small_case(B, Sq, H, D, seed=Sq + 5 * Skv + split, Skv=Skv, k_std=2.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    acc, lse_acc = ops.attn_fwd(tq, tk, tv, None, 0, split, o_dtype=dts[acc_dt])
+    o, lse = ops.attn_fwd_update(tq, tk, tv, acc, lse_acc, None, split, Skv, o_dtype=dts[out_dt])
+    f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+    ro, rl = orc.attention(*f, 1 / math.sqrt(D))
+    strict = acc_dt == "f32" and out_dt == "f32"
+    check_o(host_f64(o), ro, f32=strict, what=f"update {B, H, Sq, Skv, D, split}", vmax=vmax(v))
+    check_lse(host_f64(lse), rl, what=f"update {B, H, Sq, Skv, D, split}")
+    assert torch.equal(lse_acc, ops.attn_fwd(tq, tk, tv, None, 0, split, o_dtype=dts[acc_dt])[1]), \
+        "the running LSE must not be written when it is not the output"
+
+
+@pytest.mark.parametrize("C", [3, 4, 7])
+def test_attn_update_chain_in_place(orc, C):
+    """C chunks folded into an fp32 running result in place, the last straight into bf16: == merge kernel == oracle."""
+    B, H, S, D = 1, 3, 500, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=C * 13, k_std=3.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    edges = [(i * S) // C for i in range(C + 1)]
+    acc, lse = ops.attn_fwd(tq, tk, tv, None, edges[0], edges[1], o_dtype=torch.float32)
+    for c in range(1, C - 1):
+        ops.attn_fwd_update(tq, tk, tv, acc, lse, None, edges[c], edges[c + 1], o=acc, lse=lse)
+    o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device="cuda")
+    ops.attn_fwd_update(tq, tk, tv, acc, lse, None, edges[-2], edges[-1], o=o, lse=lse)
+    f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+    ro, rl = orc.attention(*f, 1 / math.sqrt(D))
+    check_o(host_f64(o), ro, what=f"update chain C={C}")
+    check_lse(host_f64(lse), rl, what=f"update chain C={C}")
+    om, lm = ops.dit_attention(tq, tk, tv, None, None, None, None, chunks=C, prologue=False, merge="kernel")
+    check_o(host_f64(o), host_f64(om), what="update chain vs merge kernel")
+    check_lse(host_f64(lse), host_f64(lm), what="update chain vs merge kernel")
+    ou, lu = ops.dit_attention(tq, tk, tv, None, None, None, None, chunks=C, prologue=False, merge="update")
+    assert torch.equal(ou, o) and torch.equal(lu, lse)
+
+
+def test_attn_update_causal_and_empty_rows(orc):
+    """Causal ranges in both orders: rows that see nothing in one part take the other part unchanged, and rows
+    that see nothing in either give O = 0, LSE = -inf."""
+    B, H, S, D = 1, 2, 600, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=62)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+    ro, rl = orc.attention(*f, 1 / math.sqrt(D), causal=True)
+    for first, second in [((0, 260), (260, 600)), ((260, 600), (0, 260))]:
+        acc, lse_acc = ops.attn_fwd(tq, tk, tv, None, *first, o_dtype=torch.float32, causal=True)
+        o, lse = ops.attn_fwd_update(tq, tk, tv, acc, lse_acc, None, *second, o_dtype=torch.float32, causal=True)
+        check_o(host_f64(o), ro, f32=True, what=f"causal update {first} {second}", vmax=vmax(v))
+        check_lse(host_f64(lse), rl, what=f"causal update {first} {second}")
+    # rows < 400 see no key of [400, 600): both parts empty for them
+    acc, lse_acc = ops.attn_fwd(tq, tk, tv, None, 400, 500, o_dtype=torch.float32, causal=True)
+    o, lse = ops.attn_fwd_update(tq, tk, tv, acc, lse_acc, None, 500, 600, o_dtype=torch.float32, causal=True)
+    got_o, got_l = host_f64(o), host_f64(lse)
+    assert np.all(got_o[:, :400] == 0) and np.all(np.isneginf(got_l[:, :, :400]))
+    ro2, rl2 = orc.attention(*f, 1 / math.sqrt(D), 400, 600, causal=True)
+    check_o(got_o[:, 400:], ro2[:, 400:], f32=True, what="causal update tail", vmax=vmax(v))
+    check_lse(got_l[:, :, 400:], rl2[:, :, 400:], what="causal update tail")
+
+
+def test_attn_update_strided_running_result(orc):
+    """The running result as an fp32 view into a wider buffer; nothing outside the views is written."""
+    B, S, H, D = 1, 190, 3, 64
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=45)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    acc_buf = torch.zeros((B, S, H, 2 * D), dtype=torch.float32, device="cuda")
+    acc = acc_buf[..., :D]
+    _, lse_acc = ops.attn_fwd(tq, tk, tv, None, 0, 90, o=acc)
+    o_buf = torch.zeros((B, S, H, 2 * D), dtype=torch.bfloat16, device="cuda")
+    o, lse = ops.attn_fwd_update(tq, tk, tv, acc, lse_acc, None, 90, S, o=o_buf[..., :D])
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
+    check_o(host_f64(o), ro, what="update strided")
+    check_lse(host_f64(lse), rl, what="update strided")
+    assert torch.count_nonzero(o_buf[..., D:]) == 0 and torch.count_nonzero(acc_buf[..., D:]) == 0
+
+
 def test_poll_device_error_clean():
     q, k, v, *_ = inputs.small_case(1, 128, 1, 64, seed=3)
     ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v))

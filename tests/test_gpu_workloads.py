@@ -17,6 +17,8 @@ pytestmark = pytest.mark.gpu
 
 PARTIAL = {"qwen_image": torch.float32, "qwen_image_edit": torch.float32, "wan480": torch.float32,
            "wan720": torch.bfloat16}
+# how bench.py combines the KV chunks of each workload (update: LSE merge in the attention epilogue)
+MERGE = {"qwen_image": "update", "qwen_image_edit": "update", "wan480": "kernel", "wan720": "kernel"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -33,15 +35,16 @@ def _device_compare(a: torch.Tensor, b: torch.Tensor):
     return err, cos
 
 
-@pytest.mark.parametrize("name", ["qwen_image", "qwen_image_edit", "wan480", "wan720"])
-def test_workload_parity(name):
+@pytest.mark.parametrize("name,merge", [("qwen_image", "update"), ("qwen_image", "kernel"),
+                                        ("qwen_image_edit", "update"), ("wan480", "kernel"), ("wan720", "kernel")])
+def test_workload_parity(name, merge):
     orc = oracle.get()
     inp = inputs.make_inputs(name)
     w = inp.w
     dq, dk, dv = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
     tabs = (dev_f32(inp.wq), dev_f32(inp.wk), dev_f32(inp.cos), dev_f32(inp.sin))
     o, lse = ops.dit_attention(dq, dk, dv, *tabs, eps=w.eps, chunks=w.chunks, partial_dtype=PARTIAL[name],
-                               prologue=w.prologue)
+                               prologue=w.prologue, merge=merge)
     if w.prologue:
         pq, pk = ops.qk_norm_rope(dq, dk, *tabs, eps=w.eps)
     else:
