@@ -202,6 +202,7 @@ def config_of(w, chunks, args):
             "merge": (merge_mode(w, args) + (" (fused in the last chunk's epilogue)" if merge_mode(w, args) == "update"
                                              else " (LSE-merge kernel)")) if chunks > 1 else "none",
             "prologue": w.prologue, "causal": False,
+            "launch_overlap": not getattr(args, "no_launch_overlap", False),
             "scale": "1/sqrt(D)", "l2": "flushed before every timed step (512 MiB write)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
@@ -248,6 +249,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     build.build()
     ops.load_library()
+    ops.set_launch_overlap(not args.no_launch_overlap)
 
     inp = inputs.make_inputs(args.workload)
     w = inp.w
@@ -504,6 +506,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--chunks", type=int, default=0, help="KV chunks (0: the workload's own)")
+    ap.add_argument("--no-launch-overlap", action="store_true",
+                    help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
     ap.add_argument("--merge", choices=["auto", "kernel", "update"], default="auto",
                     help="combine KV chunks by the merge kernel or in the attention epilogue (auto: the workload's)")
     ap.add_argument("--ref-rows", type=int, default=48, help="query rows per (b, h) in each reference step")

@@ -5,12 +5,15 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/ditattn.h"
 #include "internal.h"
 
 namespace {
 
 thread_local const char *g_detail = "";
+std::atomic<int> g_launch_overlap{1};
 
 dit_status fail(dit_status s, const char *why) {
   g_detail = why;
@@ -38,7 +41,16 @@ dit_status from_cuda(cudaError_t e, const char *detail) {
 
 }  // namespace
 
+bool ditattn::launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+
 extern "C" {
+
+dit_status dit_set_launch_overlap(int enable) {
+  g_detail = "";
+  if (enable != 0 && enable != 1) return fail(DIT_ERR_INVALID_ARG, "enable must be 0 or 1");
+  g_launch_overlap.store(enable, std::memory_order_relaxed);
+  return DIT_OK;
+}
 
 const char *dit_status_string(dit_status s) {
   switch (s) {

@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Update form: the O_acc tile of query tile t, half hf, is ring fill 2 * nblk + hf * kNQ + t
   // (one 128 x D bf16 tile, or two halves of an fp32 tile, per ring slot).
   const int acc_halves = kUpdate ? (args.acc_f32 ? 2 : 1) : 0;
+  griddep_wait();
+  griddep_launch_dependents();
 
   const uint32_t bars = base + L::kBar;
   const uint32_t q_full = bars;
@@ -607,8 +609,8 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
     configured[dev] = true;
   }
   dim3 grid((a.Sq + kBM * kNQ - 1) / (kBM * kNQ), a.H, B);
-  attn_fwd_kernel<D, kCausal, kUpdate><<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, to, tacc, a);
-  return cudaGetLastError();
+  return launch_kernel(attn_fwd_kernel<D, kCausal, kUpdate>, grid, dim3(kThreads), Lay::kAlloc, stream, tq, tk, tv,
+                       to, tacc, a);
 }
 
 }  // namespace

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kThreads, 4) merge_lse_kernel(const Tin *__res
   const long long q = bq % Sq, b = bq / Sq;
   const long long li = (b * H + h) * Sq + q;
   const long long off = row * D + (long long)lane * N;
+  griddep_wait();
+  griddep_launch_dependents();
 
   float mx = -INFINITY;
   for (int c = 0; c < C; ++c) mx = fmaxf(mx, lse_parts[c * psl + li]);
@@ -191,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t bars = base + kStages * kStageBytes;
   auto full = [&](int st) { return bars + 8u * st; };
   const int g = threadIdx.x / kLanes, lane = threadIdx.x % kLanes;
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kStages; ++st) mbar_init(full(st), 1);
@@ -292,9 +296,9 @@ cudaError_t launch_bulk(const void *o_parts, const float *lse_parts, int B, int 
   constexpr int kUnitRows = kStageBytes / (C * D * (int)sizeof(Tin));
   const long long n_units = (n_rows + kUnitRows - 1) / kUnitRows;
   const long long grid = n_units < 2LL * sms ? n_units : 2LL * sms;
-  merge_lse_bulk_kernel<Tin, Tout, D, C><<<(unsigned)grid, kThreads, kBulkSmem, stream>>>(
-      static_cast<const Tin *>(o_parts), lse_parts, H, Sq, n_rows, pso, psl, static_cast<Tout *>(o), lse, n_units);
-  return cudaGetLastError();
+  return launch_kernel(merge_lse_bulk_kernel<Tin, Tout, D, C>, dim3((unsigned)grid), dim3(kThreads), kBulkSmem, stream,
+                       static_cast<const Tin *>(o_parts), lse_parts, H, Sq, n_rows, pso, psl, static_cast<Tout *>(o),
+                       lse, n_units);
 }
 
 template <typename Tin, typename Tout, int D>
@@ -304,9 +308,9 @@ cudaError_t launch_typed(const void *o_parts, const float *lse_parts, int C, int
   const long long n_rows = (long long)B * Sq * H;
   const long long blocks = (n_rows + kRows - 1) / kRows;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  merge_lse_kernel<Tin, Tout, D><<<(unsigned)blocks, kThreads, 0, stream>>>(
-      static_cast<const Tin *>(o_parts), lse_parts, C, H, Sq, n_rows, pso, psl, static_cast<Tout *>(o), lse);
-  return cudaGetLastError();
+  return launch_kernel(merge_lse_kernel<Tin, Tout, D>, dim3((unsigned)blocks), dim3(kThreads), 0, stream,
+                       static_cast<const Tin *>(o_parts), lse_parts, C, H, Sq, n_rows, pso, psl,
+                       static_cast<Tout *>(o), lse);
 }
 
 template <typename Tin, typename Tout>

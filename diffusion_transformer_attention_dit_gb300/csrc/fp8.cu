@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kQThreads) quant_fp8_rows_kernel(const uint4 *
   __shared__ float red[8];
   const int nvec = K / 8;
   uint4 cur[kVec], nxt[kVec];
+  griddep_wait();
+  griddep_launch_dependents();
   long long m = blockIdx.x;
   if (m < M) q_load_row<kVec>(cur, x, m, nvec);
   for (; m < M; m += 2LL * gridDim.x) {
@@ -198,6 +200,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (kGStages + s); };
   const uint32_t acc_full = bars + 8u * (2 * kGStages);
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGStages; ++s) {
@@ -342,12 +346,10 @@ cudaError_t launch_quant_fp8_rows(const void *x, void *codes, float *scale, long
   uint2 *cc = static_cast<uint2 *>(codes);
   const int nvec = K / 8;
   if (nvec <= 2 * kQThreads)
-    quant_fp8_rows_kernel<2><<<grid, kQThreads, 0, stream>>>(xx, cc, scale, M, K);
-  else if (nvec <= 4 * kQThreads)
-    quant_fp8_rows_kernel<4><<<grid, kQThreads, 0, stream>>>(xx, cc, scale, M, K);
-  else
-    quant_fp8_rows_kernel<kQMaxVec><<<grid, kQThreads, 0, stream>>>(xx, cc, scale, M, K);
-  return cudaGetLastError();
+    return launch_kernel(quant_fp8_rows_kernel<2>, dim3(grid), dim3(kQThreads), 0, stream, xx, cc, scale, M, K);
+  if (nvec <= 4 * kQThreads)
+    return launch_kernel(quant_fp8_rows_kernel<4>, dim3(grid), dim3(kQThreads), 0, stream, xx, cc, scale, M, K);
+  return launch_kernel(quant_fp8_rows_kernel<kQMaxVec>, dim3(grid), dim3(kQThreads), 0, stream, xx, cc, scale, M, K);
 }
 
 cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,
@@ -370,8 +372,7 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
     configured[dev] = true;
   }
   dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  gemm_fp8_kernel<<<grid, kGThreads, kGSmem, stream>>>(ta, tb, to, a_scale, b_scale, M, N, K);
-  return cudaGetLastError();
+  return launch_kernel(gemm_fp8_kernel, grid, dim3(kGThreads), kGSmem, stream, ta, tb, to, a_scale, b_scale, M, N, K);
 }
 
 cudaError_t read_and_clear_fp8_error(unsigned int *value) {

@@ -7,6 +7,27 @@
 
 namespace ditattn {
 
+// Whether launches carry programmatic stream serialisation (each kernel calls
+// griddepcontrol.wait before touching global memory, so its launch and
+// preamble overlap the previous kernel's tail).  Set by dit_set_launch_overlap.
+bool launch_overlap_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_overlap_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Attention forward over keys [kv_begin, kv_end) (causal: query i sees keys j <= i).
 // Strides in elements {b, s, h}.  With o_acc non-null (update form) the result is
 // LSE-merged with the running (o_acc, lse_acc) before it is written.

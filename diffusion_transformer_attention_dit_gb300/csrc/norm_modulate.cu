@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace ditattn {
 namespace {
@@ -144,6 +145,8 @@ __global__ void __launch_bounds__(kThreads) row_norm_kernel(const uint4 *__restr
   __shared__ float red[8];
   const int nvec = C / 8;
   uint4 cur[kVec], nxt[kVec];
+  griddep_wait();
+  griddep_launch_dependents();
   long long r = blockIdx.x;
   if (r < rows) load_row<kVec>(cur, x, r, nvec);
   for (; r < rows; r += 2LL * gridDim.x) {
@@ -172,12 +175,13 @@ cudaError_t launch_rows(const void *x, const float *a, const float *c, void *y, 
   const uint4 *xx = static_cast<const uint4 *>(x);
   uint4 *yy = static_cast<uint4 *>(y);
   if (nvec <= 2 * kThreads)
-    row_norm_kernel<kLayerNorm, 2><<<grid, kThreads, 0, stream>>>(xx, yy, a, c, rows, C, L, eps);
-  else if (nvec <= 4 * kThreads)
-    row_norm_kernel<kLayerNorm, 4><<<grid, kThreads, 0, stream>>>(xx, yy, a, c, rows, C, L, eps);
-  else
-    row_norm_kernel<kLayerNorm, kMaxVec><<<grid, kThreads, 0, stream>>>(xx, yy, a, c, rows, C, L, eps);
-  return cudaGetLastError();
+    return launch_kernel(row_norm_kernel<kLayerNorm, 2>, dim3(grid), dim3(kThreads), 0, stream, xx, yy, a, c, rows, C,
+                         L, eps);
+  if (nvec <= 4 * kThreads)
+    return launch_kernel(row_norm_kernel<kLayerNorm, 4>, dim3(grid), dim3(kThreads), 0, stream, xx, yy, a, c, rows, C,
+                         L, eps);
+  return launch_kernel(row_norm_kernel<kLayerNorm, kMaxVec>, dim3(grid), dim3(kThreads), 0, stream, xx, yy, a, c, rows,
+                       C, L, eps);
 }
 
 }  // namespace

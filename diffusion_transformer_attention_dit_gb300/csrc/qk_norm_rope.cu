@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const unsigned gmask = (kLanes == 32 ? 0xffffffffu : ((1u << kLanes) - 1u)) << ((threadIdx.x & 31) & ~(kLanes - 1));
   const float inv_d = 1.0f / D;
   float w_q[8], w_k[8];
+  griddep_wait();
+  griddep_launch_dependents();
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     w_q[i] = wq[li * 8 + i];
@@ -201,12 +203,11 @@ cudaError_t launch_typed(const void *q, const void *k, void *q_out, void *k_out,
   constexpr int kRows = kUnitBytes / (D * 2);
   const long long n_units = (n_rows + kRows - 1) / kRows;
   const long long grid = n_units < 2LL * sms ? n_units : 2LL * sms;
-  qk_norm_rope_kernel<D><<<(unsigned)grid, kThreads, kSmem, stream>>>(
-      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-      static_cast<__nv_bfloat16 *>(q_out), static_cast<__nv_bfloat16 *>(k_out), wq, wk,
-      reinterpret_cast<const float4 *>(cos_tab), reinterpret_cast<const float4 *>(sin_tab), S, H, eps, n_rows,
-      n_units);
-  return cudaGetLastError();
+  return launch_kernel(qk_norm_rope_kernel<D>, dim3((unsigned)grid), dim3(kThreads), kSmem, stream,
+                       static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                       static_cast<__nv_bfloat16 *>(q_out), static_cast<__nv_bfloat16 *>(k_out), wq, wk,
+                       reinterpret_cast<const float4 *>(cos_tab), reinterpret_cast<const float4 *>(sin_tab), S, H, eps,
+                       n_rows, n_units);
 }
 
 }  // namespace

@@ -20,7 +20,8 @@ DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT 
 DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
-            "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update")
+            "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
+            "dit_set_launch_overlap")
 
 _lib = None
 
@@ -57,9 +58,10 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
                                  vp]
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
+    lib.dit_set_launch_overlap.argtypes = [i32]
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
-                 "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update"):
+                 "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -268,6 +270,12 @@ def gemm_fp8(a, a_scale, b, b_scale, out=None, stream=None):
 def poll_device_error(stream=None):
     """Synchronise the stream and raise DitError if a bounded device-side wait gave up since the last poll."""
     _check(load_library().dit_poll_device_error(_stream(stream)))
+
+
+def set_launch_overlap(enable: bool):
+    """Programmatic dependent launch for the library's kernels (default on): a kernel's launch overlaps the tail of
+    the previous kernel on its stream; every kernel waits for that kernel before touching global memory."""
+    _check(load_library().dit_set_launch_overlap(1 if enable else 0))
 
 
 def selftest_wait_timeout(stream=None):

@@ -296,6 +296,17 @@ dit_status dit_poll_device_error(struct CUstream_st *stream);
  */
 dit_status dit_selftest_wait_timeout(struct CUstream_st *stream);
 
+/*
+ * dit_set_launch_overlap -- enable (1, the default) or disable (0) programmatic
+ * dependent launch for every kernel this library launches afterwards.  When
+ * enabled, a kernel may be scheduled while the previous kernel on its stream is
+ * still finishing; each kernel waits for that kernel's completion and memory
+ * (griddepcontrol.wait) before its first global-memory access, so results are
+ * the same either way and only the launch gap shrinks.  Process-wide setting.
+ * Returns DIT_ERR_INVALID_ARG for any other value.
+ */
+dit_status dit_set_launch_overlap(int enable);
+
 /* dit_status_string -- static, human-readable name of a status code (never NULL). */
 const char *dit_status_string(dit_status s);
 

@@ -188,3 +188,9 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 8, 1, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ops.attn_fwd(q, q, q)
+
+
+def test_launch_overlap_setting(lib):
+    assert lib.dit_set_launch_overlap(2) == ops.DIT_ERR_INVALID_ARG
+    assert lib.dit_set_launch_overlap(0) == ops.DIT_OK
+    assert lib.dit_set_launch_overlap(1) == ops.DIT_OK

@@ -267,6 +267,25 @@ def test_attn_update_strided_running_result(orc):
     assert torch.count_nonzero(o_buf[..., D:]) == 0 and torch.count_nonzero(acc_buf[..., D:]) == 0
 
 
+def test_launch_overlap_gives_identical_results():
+    """Programmatic dependent launch changes only when a kernel starts: the back-to-back chain prologue ->
+    chunk attention -> update -> merge gives bit-identical results with it on and off."""
+    inp = inputs.make_inputs("tiny")
+    w = inp.w
+    args = [dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v), dev_f32(inp.wq), dev_f32(inp.wk), dev_f32(inp.cos),
+            dev_f32(inp.sin)]
+    res = {}
+    for on in (False, True):
+        ops.set_launch_overlap(on)
+        try:
+            res[on] = [ops.dit_attention(*args, eps=w.eps, chunks=4, merge=m) for m in ("update", "kernel")]
+            torch.cuda.synchronize()
+        finally:
+            ops.set_launch_overlap(True)
+    for (o0, l0), (o1, l1) in zip(res[False], res[True]):
+        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
 def test_poll_device_error_clean():
     q, k, v, *_ = inputs.small_case(1, 128, 1, 64, seed=3)
     ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v))
