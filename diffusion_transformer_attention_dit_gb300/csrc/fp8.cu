@@ -13,12 +13,13 @@
 // next row's loads before reducing the current one; the quotient is formed
 // with IEEE division and converted with cvt.rn.satfinite.e4m3x2.
 //
-// GEMM: one CTA per 128 x 256 output tile.  A TMA warp streams 128-byte K
-// blocks of A (128 rows) and B (256 rows) into a 4-stage ring (128-byte
-// swizzle); one thread issues tcgen05.mma kind::f8f6f4 (M 128, N 256, K 32 per
-// instruction) into a 256-column fp32 TMEM accumulator; four epilogue warps
-// read it back, apply the two scales, convert to bf16, stage the tile in the
-// drained ring in swizzled layout and store it with TMA.  Waits are bounded.
+// GEMM: persistent CTAs (one per SM) over 128 x 256 output tiles.  A TMA warp
+// streams 128-byte K blocks of A (128 rows) and B (256 rows) into a 4-stage
+// ring (128-byte swizzle) across tile boundaries; one thread issues
+// tcgen05.mma kind::f8f6f4 (M 128, N 256, K 32 per instruction) into one of two
+// 256-column fp32 TMEM accumulators; four epilogue warps drain the other: read
+// it back, apply the two scales, convert to bf16, stage 64-column boxes in two
+// alternating swizzled buffers and store them with TMA.  Waits are bounded.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -141,11 +142,14 @@ constexpr int kGM = 128, kGN = 256, kGK = 128;  // tile (K in bytes = elements)
 constexpr int kGStages = 4;
 constexpr int kGThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kABytes = kGM * kGK, kBBytes = kGN * kGK, kStageBytes = kABytes + kBBytes;
-constexpr int kBarOff = kGStages * kStageBytes;
-constexpr int kGNumBars = 2 * kGStages + 1;
-constexpr int kScaleOff = kBarOff + 8 * kGNumBars + 8;  // b_scale of the tile (256 floats)
-constexpr int kTmemSlotOff = kScaleOff + 4 * kGN;
+constexpr int kOutBox = kGM * 128;                  // one output box: 128 rows x 64 bf16 columns
+constexpr int kOutOff = kGStages * kStageBytes;     // two output boxes, alternating
+constexpr int kBarOff = kOutOff + 2 * kOutBox;
+// full[kGStages], empty[kGStages], acc_full[2], acc_empty[2], drain
+constexpr int kGNumBars = 2 * kGStages + 5;
+constexpr int kTmemSlotOff = kBarOff + 8 * kGNumBars;
 constexpr int kGSmem = kTmemSlotOff + 16 + 1024;
+constexpr uint32_t kGTmemCols = 2 * kGN;  // two accumulators: the epilogue drains one while the MMAs fill the other
 
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4)                                  /* D format: f32 */
@@ -183,6 +187,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Persistent: CTA c takes output tiles c, c + gridDim.x, ... (N fastest).  The
+// producer streams the K blocks of all its tiles through one ring; the MMA
+// thread accumulates tile i into TMEM buffer i % 2 and the epilogue warps drain
+// buffer i % 2 while the MMAs of tile i + 1 fill the other.
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ a_scale,
@@ -190,16 +198,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *sbase = smem_raw + (base - raw);
-  float *s_bscale = reinterpret_cast<float *>(sbase + kScaleOff);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + kTmemSlotOff);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + (base - raw) + kTmemSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kGN, m0 = blockIdx.y * kGM;
   const int nk = (K + kGK - 1) / kGK;
+  const int tiles_n = (N + kGN - 1) / kGN;
+  const int n_tiles = tiles_n * ((M + kGM - 1) / kGM);
   const uint32_t bars = base + kBarOff;
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (kGStages + s); };
-  const uint32_t acc_full = bars + 8u * (2 * kGStages);
+  auto acc_full = [&](int b) { return bars + 8u * (2 * kGStages + b); };
+  auto acc_empty = [&](int b) { return bars + 8u * (2 * kGStages + 2 + b); };
+  const uint32_t drain = bars + 8u * (2 * kGStages + 4);
   griddep_wait();
   griddep_launch_dependents();
 
@@ -208,13 +217,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 128);  // every epilogue thread, after its last TMEM read of the buffer
+    }
+    mbar_init(drain, 1);
     mbar_fence_init();
   }
-  if (warp >= 2)  // epilogue warps stage this tile's column scales
-    for (int i = threadIdx.x - 64; i < kGN; i += 128) s_bscale[i] = n0 + i < N ? b_scale[n0 + i] : 0.f;
   if (warp == 1) {
-    tmem_alloc(base + kTmemSlotOff, 256);
+    tmem_alloc(base + kTmemSlotOff, kGTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -223,83 +234,130 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kGStages;
-        if (!wait_bounded(empty(s), ((kb / kGStages) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(full(s), kStageBytes);
-        tma_load_2d(base + s * kStageBytes, &tm_a, full(s), kb * kGK, m0);
-        tma_load_2d(base + s * kStageBytes + kABytes, &tm_b, full(s), kb * kGK, n0);
-        ++issued;
+      uint32_t g = 0;  // K blocks issued over all tiles
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kGN;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % kGStages;
+          if (!wait_bounded(empty(s), ((g / kGStages) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full(s), kStageBytes);
+          tma_load_2d(base + s * kStageBytes, &tm_a, full(s), kb * kGK, m0);
+          tma_load_2d(base + s * kStageBytes + kABytes, &tm_b, full(s), kb * kGK, n0);
+        }
       }
-      for (int i = issued > kGStages ? issued - kGStages : 0; i < issued; ++i)
+      // every copy issued must land before the CTA may exit
+      for (uint32_t i = g > kGStages ? g - kGStages : 0; i < g; ++i)
         wait_bounded(full(i % kGStages), (i / kGStages) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kGM, kGN);
+      uint32_t g = 0;
       bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % kGStages;
-        ok = wait_bounded(full(s), (kb / kGStages) & 1);
+      int i = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++i) {
+        const int buf = i & 1;
+        ok = wait_bounded(acc_empty(buf), ((i >> 1) & 1) ^ 1);  // the epilogue has drained this buffer
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t a0 = base + s * kStageBytes, b0 = a0 + kABytes;
+        const uint32_t d = tmem + buf * kGN;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % kGStages;
+          ok = wait_bounded(full(s), (g / kGStages) & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint32_t a0 = base + s * kStageBytes, b0 = a0 + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kGK / 32; ++kk)
-          mma_f8(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc,
-                 (kb > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(empty(s));
+          for (int kk = 0; kk < kGK / 32; ++kk)
+            mma_f8(d, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(empty(s));
+        }
+        if (ok) tc_commit(acc_full(buf));
       }
-      tc_commit(acc_full);  // also drains: every MMA issued has completed when this fires
-      wait_bounded(acc_full, 0);
+      // every MMA issued must complete before TMEM is freed
+      tc_commit(drain);
+      wait_bounded(drain, 0);
     }
     __syncwarp();
   } else {
-    // epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 (one output row per thread)
+    // ------------------------------------------------------------ epilogue
+    // warp w reads TMEM lanes 32 * (w % 4) .. + 31: one output row per thread
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const bool ok = named_barrier_and(1, 128, wait_bounded(acc_full, 0));
-    if (ok) {
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t sw = row & 7;
+    bool ok = true;
+    int i = 0;
+    int last_buf = -1;  // (row 0) staging buffer read by the most recently committed store
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
+      const int buf = i & 1;
+      const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kGN;
+      ok = named_barrier_and(1, 128, ok && wait_bounded(acc_full(buf), (i >> 1) & 1));
+      if (!ok) break;
       tc_fence_after_sync();
       const float as = m0 + row < M ? a_scale[m0 + row] : 0.f;
-      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-      const uint32_t sw = row & 7;
-      // the drained ring holds the bf16 tile: box c (64 columns) at c * 16 KB, 128-byte rows, swizzled
 #pragma unroll 1
       for (int c = 0; c < kGN / 32; ++c) {
+        const int box = c >> 1;  // 64 output columns per box, staged in buffer box % 2
+        const uint32_t stage = base + kOutOff + (box & 1) * kOutBox;
+        if ((c & 1) == 0) {
+          // every earlier store that reads this staging buffer must be done with it: all but the most
+          // recent store, or all of them if the most recent one reads this buffer too (boxes past N
+          // are skipped, so the buffers need not alternate between stores)
+          if (row == 0) {
+            if (last_buf == (box & 1))
+              bulk_wait_read_all();
+            else
+              bulk_wait_read_all_but_one();
+          }
+          named_barrier_sync(1, 128);
+        }
         uint32_t o[32];
-        tmem_ld_x32(tmem + lane_base + c * 32, o);
-        const uint32_t dst = base + (c >> 1) * 16384 + row * 128;
+        tmem_ld_x32(tmem + lane_base + buf * kGN + c * 32, o);
+        const int col0 = n0 + c * 32;
+        float bs[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) bs[j] = col0 + j < N ? __ldg(b_scale + col0 + j) : 0.f;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int col = c * 32 + 8 * u + 2 * e;
-            w[e] = pack_bf16(__uint_as_float(o[8 * u + 2 * e]) * as * s_bscale[col],
-                             __uint_as_float(o[8 * u + 2 * e + 1]) * as * s_bscale[col + 1]);
+            const int j = 8 * u + 2 * e;
+            w[e] = pack_bf16(__uint_as_float(o[j]) * as * bs[j], __uint_as_float(o[j + 1]) * as * bs[j + 1]);
           }
-          st_shared_v4(dst + ((((c & 1) * 4 + u) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+          st_shared_v4(stage + row * 128 + ((((c & 1) * 4 + u) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        }
+        if (c & 1) {
+          fence_proxy_async_smem();
+          named_barrier_sync(1, 128);
+          if (row == 0 && n0 + box * 64 < N) {
+            tma_store_2d(&tm_o, stage, n0 + box * 64, m0);
+            bulk_commit_group();
+            last_buf = box & 1;
+          }
         }
       }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 128);
-      if (row == 0) {
-        for (int c = 0; c < kGN / 64; ++c)
-          if (n0 + c * 64 < N) tma_store_2d(&tm_o, base + c * 16384, n0 + c * 64, m0);
-        bulk_commit_group();
-        bulk_wait_read_all();
-      }
+      // this thread's reads of the buffer are complete (each TMEM load waits): hand it back
+      tc_fence_before_sync();
+      mbar_arrive(acc_empty(buf));
     }
+    if (row == 0) bulk_wait_read_all();
   }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, kGTmemCols);
   }
 }
 
@@ -371,8 +429,13 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  return launch_kernel(gemm_fp8_kernel, grid, dim3(kGThreads), kGSmem, stream, ta, tb, to, a_scale, b_scale, M, N, K);
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + kGM - 1) / kGM);
+  const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);  // one persistent CTA per SM
+  return launch_kernel(gemm_fp8_kernel, dim3(grid), dim3(kGThreads), kGSmem, stream, ta, tb, to, a_scale, b_scale, M,
+                       N, K);
 }
 
 cudaError_t read_and_clear_fp8_error(unsigned int *value) {

@@ -425,29 +425,55 @@ def test_quant_fp8_rows_bit_exact(orc, M, K):
     assert np.array_equal(codes.cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 264, 208), (1, 8, 16), (520, 768, 1024)])
+def _fp8_operands(orc, M, N, K, seed, a_std=2.0, b_std=0.05):
+    """Seeded bf16 activations and weights quantised by the oracle (host); codes and scales go to the GPU."""
+    xa = inputs.bf16_normal(M * K, seed=seed, std=a_std).reshape(M, K)
+    xb = inputs.bf16_normal(N * K, seed=seed + 1, std=b_std).reshape(N, K)
+    a, sa = orc.quant_fp8_rows(inputs.bf16_bits_to_f64(xa))
+    b, sb = orc.quant_fp8_rows(inputs.bf16_bits_to_f64(xb))
+    dev = [torch.from_numpy(np.ascontiguousarray(t)).cuda() for t in (a, sa, b, sb)]
+    return (a, sa, b, sb), dev
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 264, 208), (1, 8, 16), (520, 768, 1024),
+                                   (4100, 1288, 256)])  # the last: 198 tiles, so CTAs take two, ragged N
 def test_gemm_fp8_parity(orc, M, N, K):
-    xa = inputs.bf16_normal(M * K, seed=M + K, std=2.0).reshape(M, K)
-    xb = inputs.bf16_normal(N * K, seed=N + 3 * K, std=0.05).reshape(N, K)
-    a, sa = ops.quant_fp8_rows(dev_bf16(xa))
-    b, sb = ops.quant_fp8_rows(dev_bf16(xb))
-    out = ops.gemm_fp8(a, sa, b, sb)
-    ref = orc.gemm_fp8(a.cpu().numpy(), sa.cpu().numpy(), b.cpu().numpy(), sb.cpu().numpy())
+    (a, sa, b, sb), (da, dsa, db, dsb) = _fp8_operands(orc, M, N, K, seed=M + 3 * N + K)
+    out = ops.gemm_fp8(da, dsa, db, dsb)
+    ref = orc.gemm_fp8(a, sa, b, sb)
     # fp32 accumulation of exact e4m3 products, two fp32 scale multiplies, one bf16 rounding
     check_bf16_rounding(host_f64(out), ref, "fp8 gemm", atol=1e-5 * np.abs(ref).max())
 
 
 def test_gemm_fp8_strided_output(orc):
     M, N, K = 130, 72, 64
-    xa = inputs.bf16_normal(M * K, seed=5).reshape(M, K)
-    xb = inputs.bf16_normal(N * K, seed=6).reshape(N, K)
-    a, sa = ops.quant_fp8_rows(dev_bf16(xa))
-    b, sb = ops.quant_fp8_rows(dev_bf16(xb))
+    (a, sa, b, sb), (da, dsa, db, dsb) = _fp8_operands(orc, M, N, K, seed=5, a_std=1.0, b_std=1.0)
     buf = torch.zeros((M, N + 40), dtype=torch.bfloat16, device="cuda")
-    ops.gemm_fp8(a, sa, b, sb, out=buf[:, :N])
-    ref = orc.gemm_fp8(a.cpu().numpy(), sa.cpu().numpy(), b.cpu().numpy(), sb.cpu().numpy())
+    ops.gemm_fp8(da, dsa, db, dsb, out=buf[:, :N])
+    ref = orc.gemm_fp8(a, sa, b, sb)
     check_bf16_rounding(host_f64(buf[:, :N]), ref, "fp8 gemm strided", atol=1e-5 * np.abs(ref).max())
     assert torch.count_nonzero(buf[:, N:]) == 0
+
+
+def test_gemm_fp8_qkv_projection_full_size(orc):
+    """The Qwen-Image-Edit QKV projection (17248 tokens x 9216 x 3072) in the launch bench.py times: every CTA
+    runs 32 tiles; sampled output rows against the oracle."""
+    M, N, K = 17248, 9216, 3072
+    # any e4m3 codes are valid GEMM operands: seeded random bytes (NaN codes replaced) and scales
+    rng = np.random.default_rng(97)
+    a = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0x38
+    b[(b & 0x7F) == 0x7F] = 0x38
+    sa = rng.uniform(1e-3, 1e-2, M).astype(np.float32)
+    sb = rng.uniform(1e-4, 1e-3, N).astype(np.float32)
+    da, dsa, db, dsb = (torch.from_numpy(t).cuda() for t in (a, sa, b, sb))
+    out = ops.gemm_fp8(da, dsa, db, dsb)
+    from parity import sample_rows
+    rows = sample_rows(M, 40, seed=3)
+    ref = orc.gemm_fp8(np.ascontiguousarray(a[rows]), np.ascontiguousarray(sa[rows]), b, sb)
+    got = host_f64(out[torch.from_numpy(rows).cuda()])
+    check_bf16_rounding(got, ref, "fp8 gemm full size", atol=1e-5 * np.abs(ref).max())
 
 
 def test_w8a8_projection_accuracy():
