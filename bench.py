@@ -42,9 +42,11 @@ PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480
 # specifies per-chunk bf16 partials merged by the merge kernel).
 MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", "wan480": "kernel",
          "wan720": "kernel"}
-# DRAM bytes per attention launch (read + write) from an ncu capture of the bench step
-# (profiles/launch_list_qwen_image_step.md), valid for the attention source it was taken on.
-ATTN_TRAFFIC = {"source_sha256_prefix": "9fcb952b8c9608e4", "qwen_image": (39.3 + 56.2) * 1e6}
+# DRAM bytes (read + write) of the attention launches of one bench step, from an ncu capture
+# (profiles/launch_list_qwen_image_step.md): chunk 0 (fp32 running O) and chunk 1 (update form,
+# bf16 O), averaged per launch; valid for the attention source it was taken on.
+ATTN_TRAFFIC = {"source_sha256_prefix": "d14dc776a121871c",
+                "qwen_image": ((28.31 + 53.60) + (97.33 + 58.85)) / 2 * 1e6}
 
 
 def peaks():
@@ -432,8 +434,7 @@ def run_ring_overlap(args):
         kr = torch.cat([a for a, _ in remote], dim=1)
         vr = torch.cat([b for _, b in remote], dim=1)
         o1, l1 = ops.attn_fwd(q, k_loc, v_loc, o_dtype=torch.float32)
-        o2, l2 = ops.attn_fwd(q, kr, vr, o_dtype=torch.float32)
-        return ops.attn_merge_lse(torch.stack([o1, o2]), torch.stack([l1, l2]))
+        return ops.attn_fwd_update(q, kr, vr, o1, l1, lse=l1)
 
     def overlapped():
         return ops.ring_overlap_attention(q, k_loc, v_loc, remote, gather_stream=side)

@@ -321,8 +321,9 @@ def ring_overlap_attention(q, k_local, v_local, remote_kv, scale: float | None =
     Attention over the local K/V runs on the current stream while the remote K/V
     chunks are gathered into one contiguous buffer on `gather_stream` (device
     copies stand in for the all-gather of a multi-GPU run); then one attention
-    over the gathered chunks and an LSE merge of the two results.  remote_kv is
-    a list of (k_i, v_i) tensors [B, S_i, H, D].  Returns (o, lse).
+    over the gathered chunks whose epilogue LSE-merges it into the local result
+    (the update_out_and_lse step).  remote_kv is a list of (k_i, v_i) tensors
+    [B, S_i, H, D].  Returns (o, lse).
     """
     main = torch.cuda.current_stream()
     side = gather_stream if gather_stream is not None else torch.cuda.Stream(device=q.device)
@@ -335,10 +336,7 @@ def ring_overlap_attention(q, k_local, v_local, remote_kv, scale: float | None =
         gathered.record(side)
     k_r.record_stream(main)
     v_r.record_stream(main)
-    o_parts = torch.empty((2, B, Sq, H, D), dtype=partial_dtype, device=q.device)
-    lse_parts = torch.empty((2, B, H, Sq), dtype=torch.float32, device=q.device)
-    attn_fwd(q, k_local, v_local, scale, o=o_parts[0], lse=lse_parts[0])
+    acc, lse = attn_fwd(q, k_local, v_local, scale, o_dtype=partial_dtype)
     main.wait_event(gathered)
-    attn_fwd(q, k_r, v_r, scale, o=o_parts[1], lse=lse_parts[1])
-    return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype)
+    return attn_fwd_update(q, k_r, v_r, acc, lse, scale, o_dtype=out_dtype, lse=lse)
 
