@@ -460,6 +460,77 @@ def run_ring_overlap(args):
                       "attention_tflops_overlapped": w.attention_flops() / res["overlapped"] / 1e9}))
 
 
+def run_hbm_kernels(args):
+    """Diagnostic: each HBM-bound kernel alone at the workload's shapes (synthetic inputs, L2 flushed before every
+    timed launch, CUDA events, median of the steps): prologue, LSE merge of the workload's chunk count (8 for a
+    one-chunk workload), LayerNorm-modulate and RMSNorm over C = H*D, fp8 quantiser.  Achieved = algorithmic bytes /
+    time."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import build, ops
+
+    build.build()
+    ops.load_library()
+    ops.set_launch_overlap(not args.no_launch_overlap)
+    w = inputs.WORKLOADS[args.workload]
+    B, S, H, D = w.B, w.S, w.H, w.D
+    C = w.chunks if w.chunks > 1 else 8
+    pdt = torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + w.index)
+    rnd = lambda *shape: torch.randn(*shape, device=dev, generator=g)  # noqa: E731
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        ts = []
+        for _ in range(max(args.steps, 5)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        ops.poll_device_error()
+        return statistics.median(ts)
+
+    peak_tf, peak_gbs, src = peaks()
+    res = {}
+
+    def record(name, us, nbytes):
+        gbs = nbytes / us / 1e3
+        res[name] = {"us": us, "GB": nbytes / 1e9, "GB/s": gbs, "frac": gbs / peak_gbs}
+
+    q, k = rnd(B, S, H, D).to(torch.bfloat16), rnd(B, S, H, D).to(torch.bfloat16)
+    wq, wk = 1 + 0.1 * rnd(D), 1 + 0.1 * rnd(D)
+    cos, sin = rnd(S, D // 2), rnd(S, D // 2)
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    record("qk_norm_rope", timed(lambda: ops.qk_norm_rope(q, k, wq, wk, cos, sin, w.eps, q_out=qo, k_out=ko)),
+           8 * B * S * H * D + 4 * S * D + 8 * D)
+    del k, ko
+    parts = rnd(C, B, S, H, D).to(pdt)
+    lse_parts = 3 + 2 * rnd(C, B, H, S)
+    lse = torch.empty(B, H, S, device=dev)
+    record(f"merge_lse C={C} {PARTIAL[w.name]}->bf16", timed(lambda: ops.attn_merge_lse(parts, lse_parts, o=qo, lse=lse)),
+           C * B * S * H * D * parts.element_size() + 4 * C * B * H * S + 2 * B * S * H * D + 4 * B * H * S)
+    del parts, lse_parts
+    x, y = q.view(B, S, H * D), qo.view(B, S, H * D)
+    Cc = H * D
+    sc, sh, wn = 0.1 * rnd(B, Cc), 0.1 * rnd(B, Cc), 1 + 0.1 * rnd(Cc)
+    record("layer_norm_modulate", timed(lambda: ops.layer_norm_modulate(x, sc, sh, w.eps, y=y)),
+           4 * B * S * Cc + 8 * B * Cc)
+    record("rms_norm (over C)", timed(lambda: ops.rms_norm(x, wn, w.eps, y=y)), 4 * B * S * Cc + 4 * Cc)
+    codes = torch.empty((B * S, Cc), dtype=torch.uint8, device=dev)
+    scales = torch.empty(B * S, dtype=torch.float32, device=dev)
+    record("quant_fp8_rows", timed(lambda: ops.quant_fp8_rows(x.view(B * S, Cc), codes, scales)),
+           3 * B * S * Cc + 4 * B * S)
+    print(json.dumps({"mode": "hbm_kernels", "workload": w.name, "peak_GBps": peak_gbs, "peak_source": src,
+                      "kernels": res}))
+
+
 def run_qkv_fp8(args):
     """Diagnostic: per-token e4m3 quantisation of the tokens (B*S x H*D) and the fp8 GEMM with a
     [3*H*D, H*D] QKV weight, synthetic, timed with CUDA events (L2 flushed before each step)."""
@@ -516,6 +587,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ring-overlap", type=int, default=0, metavar="RANKS",
                     help="time the one-GPU ring-overlap emulation with RANKS key shards instead (diagnostic)")
+    ap.add_argument("--hbm-kernels", action="store_true",
+                    help="time each HBM-bound kernel alone at the workload's shapes instead (diagnostic)")
     ap.add_argument("--qkv-fp8", action="store_true",
                     help="time the W8A8 fp8 QKV projection of the workload's tokens instead (diagnostic)")
     ap.add_argument("--traffic", type=float, default=None,
@@ -531,6 +604,8 @@ def main():
         run_ring_overlap(args)
     elif args.qkv_fp8:
         run_qkv_fp8(args)
+    elif args.hbm_kernels:
+        run_hbm_kernels(args)
     else:
         run_ours(args)
 

@@ -393,21 +393,37 @@ bool encode_2d(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es
 
 int quant_fp8_max_k() { return kQMaxVec * 8 * kQThreads; }
 
-cudaError_t launch_quant_fp8_rows(const void *x, void *codes, float *scale, long long M, int K, cudaStream_t stream) {
-  int dev = 0, sms = 0;
+namespace {
+
+// Persistent grid sized by occupancy (capped at 8 CTAs per SM); kVec as for the row norms.
+template <int kVec>
+cudaError_t launch_quant_vec(const uint4 *x, uint2 *codes, float *scale, long long M, int K, cudaStream_t stream) {
+  int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_fp8_rows_kernel<kVec>, kQThreads, 0);
   if (e != cudaSuccess) return e;
-  const long long cap = 8LL * sms;  // persistent CTAs
+  const long long cap = (long long)(per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm) * sms;
   const unsigned grid = static_cast<unsigned>(M < cap ? M : cap);
+  return launch_kernel(quant_fp8_rows_kernel<kVec>, dim3(grid), dim3(kQThreads), 0, stream, x, codes, scale, M, K);
+}
+
+}  // namespace
+
+cudaError_t launch_quant_fp8_rows(const void *x, void *codes, float *scale, long long M, int K, cudaStream_t stream) {
   const uint4 *xx = static_cast<const uint4 *>(x);
   uint2 *cc = static_cast<uint2 *>(codes);
-  const int nvec = K / 8;
-  if (nvec <= 2 * kQThreads)
-    return launch_kernel(quant_fp8_rows_kernel<2>, dim3(grid), dim3(kQThreads), 0, stream, xx, cc, scale, M, K);
-  if (nvec <= 4 * kQThreads)
-    return launch_kernel(quant_fp8_rows_kernel<4>, dim3(grid), dim3(kQThreads), 0, stream, xx, cc, scale, M, K);
-  return launch_kernel(quant_fp8_rows_kernel<kQMaxVec>, dim3(grid), dim3(kQThreads), 0, stream, xx, cc, scale, M, K);
+  switch ((K / 8 + kQThreads - 1) / kQThreads) {
+    case 1: return launch_quant_vec<1>(xx, cc, scale, M, K, stream);
+    case 2: return launch_quant_vec<2>(xx, cc, scale, M, K, stream);
+    case 3: return launch_quant_vec<3>(xx, cc, scale, M, K, stream);
+    case 4: return launch_quant_vec<4>(xx, cc, scale, M, K, stream);
+    case 5: return launch_quant_vec<5>(xx, cc, scale, M, K, stream);
+    case 6: return launch_quant_vec<6>(xx, cc, scale, M, K, stream);
+    case 7: return launch_quant_vec<7>(xx, cc, scale, M, K, stream);
+    default: return launch_quant_vec<kQMaxVec>(xx, cc, scale, M, K, stream);
+  }
 }
 
 cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,

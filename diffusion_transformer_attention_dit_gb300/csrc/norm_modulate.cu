@@ -11,10 +11,13 @@
 // fp32 arithmetic, one bf16 rounding.
 //
 // HBM-bound (2 bytes read + 2 written per element).  A row is spread over 128
-// threads as 16-byte vectors held in registers (C <= 8192, C a multiple of 8),
-// so the two passes (mean, then the squared deviations) read HBM once.
-// Persistent CTAs (8 per SM) issue the next row's loads before reducing the
-// current one.
+// threads as 16-byte vectors held in registers (C <= 8192, C a multiple of 8)
+// and read from HBM once.  LayerNorm takes the mean and variance in one
+// reduction of the sums of (x - K) and (x - K)^2 with K the row's first
+// element (the shifted-data form of the variance, which avoids the
+// cancellation of E[x^2] - mean^2 when |mean| >> std): one barrier per row, as
+// RMSNorm.  Persistent CTAs (8 per SM) issue the next row's loads before
+// reducing the current one.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,10 +36,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Sum over the CTA; every thread gets the result.  `red` holds 4 floats.  One
-// barrier per call: the callers alternate between two `red` buffers, and the
-// barrier of the next call on the other buffer orders each buffer's reads
-// before its next writes.
+// Sums over the CTA; every thread gets the results.  `red` holds 4 floats per
+// value.  One barrier per call: the callers alternate between two `red`
+// buffers, and the barrier of the next call on the other buffer orders each
+// buffer's reads before its next writes.
 __device__ __forceinline__ float block_sum(float v, float *red) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -44,12 +47,25 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   __syncthreads();
   return (red[0] + red[1]) + (red[2] + red[3]);
 }
+__device__ __forceinline__ float2 block_sum2(float v, float w, float *red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    v += __shfl_xor_sync(0xffffffffu, v, off);
+    w += __shfl_xor_sync(0xffffffffu, w, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = v;
+    red[4 + (threadIdx.x >> 5)] = w;
+  }
+  __syncthreads();
+  return make_float2((red[0] + red[1]) + (red[2] + red[3]), (red[4] + red[5]) + (red[6] + red[7]));
+}
 
 // Normalise one row whose 16-byte vectors this thread holds in `raw`, and store it.
 template <bool kLayerNorm, int kVec>
-__device__ __forceinline__ void norm_row(const uint4 (&raw)[kVec], uint4 *y, const float *__restrict__ a,
-                                         const float *__restrict__ c, long long r, int nvec, int C, int L, float eps,
-                                         float *red) {
+__device__ __forceinline__ void norm_row(const uint4 (&raw)[kVec], uint32_t first, uint4 *y,
+                                         const float *__restrict__ a, const float *__restrict__ c, long long r,
+                                         int nvec, int C, int L, float eps, float *red) {
   const float inv_c = 1.0f / C;
   float v[kVec][8];
 #pragma unroll
@@ -63,20 +79,22 @@ __device__ __forceinline__ void norm_row(const uint4 (&raw)[kVec], uint4 *y, con
   }
   float inv, mu = 0.f;
   if (kLayerNorm) {
-    float s = 0.f;
+    // shifted sums: K = the row's first element (every thread loaded it with the row)
+    const float K = __uint_as_float(first << 16);
+    float s = 0.f, ss = 0.f;
 #pragma unroll
     for (int u = 0; u < kVec; ++u)
       if (threadIdx.x + u * kThreads < nvec)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s += v[u][e];
-    mu = block_sum(s, red) * inv_c;
-    float ss = 0.f;
-#pragma unroll
-    for (int u = 0; u < kVec; ++u)
-      if (threadIdx.x + u * kThreads < nvec)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(v[u][e] - mu, v[u][e] - mu, ss);
-    inv = rsqrtf(fmaf(block_sum(ss, red + 4), inv_c, eps));
+        for (int e = 0; e < 8; ++e) {
+          const float d = v[u][e] - K;
+          s += d;
+          ss = fmaf(d, d, ss);
+        }
+    const float2 t = block_sum2(s, ss, red);
+    const float dm = t.x * inv_c;  // mean - K
+    mu = K + dm;
+    inv = rsqrtf(fmaxf(fmaf(t.y, inv_c, -dm * dm), 0.f) + eps);
   } else {
     float ss = 0.f;
 #pragma unroll
@@ -126,13 +144,16 @@ __device__ __forceinline__ void norm_row(const uint4 (&raw)[kVec], uint4 *y, con
   }
 }
 
-template <int kVec>
-__device__ __forceinline__ void load_row(uint4 (&raw)[kVec], const uint4 *__restrict__ x, long long r, int nvec) {
+template <bool kLayerNorm, int kVec>
+__device__ __forceinline__ void load_row(uint4 (&raw)[kVec], uint32_t &first, const uint4 *__restrict__ x,
+                                         long long r, int nvec) {
 #pragma unroll
   for (int u = 0; u < kVec; ++u) {
     const int i = threadIdx.x + u * kThreads;
     if (i < nvec) raw[u] = __ldcs(x + r * nvec + i);
   }
+  // the row's first element (LayerNorm's shift), one broadcast load per warp
+  if (kLayerNorm) first = __ldg(reinterpret_cast<const unsigned int *>(x + r * nvec));
 }
 
 // Persistent CTAs walk rows r = blockIdx.x, + gridDim.x, ...; the next row's
@@ -142,46 +163,60 @@ template <bool kLayerNorm, int kVec>
 __global__ void __launch_bounds__(kThreads) row_norm_kernel(const uint4 *__restrict__ x, uint4 *y,
                                                             const float *__restrict__ a, const float *__restrict__ c,
                                                             long long rows, int C, int L, float eps) {
-  __shared__ float red[8];
+  __shared__ float red[16];
   const int nvec = C / 8;
   uint4 cur[kVec], nxt[kVec];
+  uint32_t fcur = 0, fnxt = 0;
   griddep_wait();
   griddep_launch_dependents();
   long long r = blockIdx.x;
-  if (r < rows) load_row<kVec>(cur, x, r, nvec);
+  if (r < rows) load_row<kLayerNorm, kVec>(cur, fcur, x, r, nvec);
+  // one barrier per row: consecutive rows alternate between red[0..7] and red[8..15]
   for (; r < rows; r += 2LL * gridDim.x) {
     const long long r1 = r + gridDim.x;
-    if (r1 < rows) load_row<kVec>(nxt, x, r1, nvec);
-    // LayerNorm rows use red[0..3] and red[4..7] (two barriers per row); RMSNorm
-    // rows (one barrier each) alternate between them
-    norm_row<kLayerNorm, kVec>(cur, y, a, c, r, nvec, C, L, eps, red);
+    if (r1 < rows) load_row<kLayerNorm, kVec>(nxt, fnxt, x, r1, nvec);
+    norm_row<kLayerNorm, kVec>(cur, fcur, y, a, c, r, nvec, C, L, eps, red);
     if (r1 >= rows) break;
     const long long r2 = r1 + gridDim.x;
-    if (r2 < rows) load_row<kVec>(cur, x, r2, nvec);
-    norm_row<kLayerNorm, kVec>(nxt, y, a, c, r1, nvec, C, L, eps, kLayerNorm ? red : red + 4);
+    if (r2 < rows) load_row<kLayerNorm, kVec>(cur, fcur, x, r2, nvec);
+    norm_row<kLayerNorm, kVec>(nxt, fnxt, y, a, c, r1, nvec, C, L, eps, red + 8);
   }
 }
 
+// Persistent grid: as many CTAs as can be resident (registers decide, since a
+// thread holds kVec row vectors twice), capped at 8 per SM.
+template <bool kLayerNorm, int kVec>
+cudaError_t launch_rows_vec(const uint4 *x, const float *a, const float *c, uint4 *y, long long rows, int C, int L,
+                            float eps, cudaStream_t stream) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_norm_kernel<kLayerNorm, kVec>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const long long cap = (long long)(per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm) * sms;
+  const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
+  return launch_kernel(row_norm_kernel<kLayerNorm, kVec>, dim3(grid), dim3(kThreads), 0, stream, x, y, a, c, rows, C,
+                       L, eps);
+}
+
+// kVec = the number of 16-byte vectors each of the 128 threads holds: exactly
+// ceil(C / 8 / 128), so no registers go to vectors past the row's end.
 template <bool kLayerNorm>
 cudaError_t launch_rows(const void *x, const float *a, const float *c, void *y, long long rows, int C, int L,
                         float eps, cudaStream_t stream) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const long long cap = 8LL * sms;  // persistent CTAs
-  const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
-  const int nvec = C / 8;
   const uint4 *xx = static_cast<const uint4 *>(x);
   uint4 *yy = static_cast<uint4 *>(y);
-  if (nvec <= 2 * kThreads)
-    return launch_kernel(row_norm_kernel<kLayerNorm, 2>, dim3(grid), dim3(kThreads), 0, stream, xx, yy, a, c, rows, C,
-                         L, eps);
-  if (nvec <= 4 * kThreads)
-    return launch_kernel(row_norm_kernel<kLayerNorm, 4>, dim3(grid), dim3(kThreads), 0, stream, xx, yy, a, c, rows, C,
-                         L, eps);
-  return launch_kernel(row_norm_kernel<kLayerNorm, kMaxVec>, dim3(grid), dim3(kThreads), 0, stream, xx, yy, a, c, rows,
-                       C, L, eps);
+  switch ((C / 8 + kThreads - 1) / kThreads) {
+    case 1: return launch_rows_vec<kLayerNorm, 1>(xx, a, c, yy, rows, C, L, eps, stream);
+    case 2: return launch_rows_vec<kLayerNorm, 2>(xx, a, c, yy, rows, C, L, eps, stream);
+    case 3: return launch_rows_vec<kLayerNorm, 3>(xx, a, c, yy, rows, C, L, eps, stream);
+    case 4: return launch_rows_vec<kLayerNorm, 4>(xx, a, c, yy, rows, C, L, eps, stream);
+    case 5: return launch_rows_vec<kLayerNorm, 5>(xx, a, c, yy, rows, C, L, eps, stream);
+    case 6: return launch_rows_vec<kLayerNorm, 6>(xx, a, c, yy, rows, C, L, eps, stream);
+    case 7: return launch_rows_vec<kLayerNorm, 7>(xx, a, c, yy, rows, C, L, eps, stream);
+    default: return launch_rows_vec<kLayerNorm, kMaxVec>(xx, a, c, yy, rows, C, L, eps, stream);
+  }
 }
 
 }  // namespace
