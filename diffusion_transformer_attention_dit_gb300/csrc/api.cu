@@ -42,6 +42,7 @@ dit_status from_cuda(cudaError_t e, const char *detail) {
 }  // namespace
 
 bool ditattn::launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+void ditattn::set_error_detail(const char *why) { g_detail = why; }
 
 extern "C" {
 

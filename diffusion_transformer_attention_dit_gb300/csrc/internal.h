@@ -12,6 +12,9 @@ namespace ditattn {
 // preamble overlap the previous kernel's tail).  Set by dit_set_launch_overlap.
 bool launch_overlap_enabled();
 
+// Set the text dit_last_error_detail returns (for entry points outside api.cu).
+void set_error_detail(const char *why);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                           Args... args) {

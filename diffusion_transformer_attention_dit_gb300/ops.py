@@ -21,7 +21,7 @@ DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
-            "dit_set_launch_overlap")
+            "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace")
 
 _lib = None
 
@@ -59,9 +59,14 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
     lib.dit_set_launch_overlap.argtypes = [i32]
+    lib.dit_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, vp,
+                                       i32, vp, vp, ctypes.c_size_t, vp]
+    lib.dit_attention_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.dit_attention_host_workspace.restype = ctypes.c_size_t
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
-                 "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap"):
+                 "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap",
+                 "dit_attention_host"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -311,6 +316,56 @@ def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1,
     for c in range(chunks):
         attn_fwd(q, k, v, scale, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c], stream=stream)
     return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype, stream=stream)
+
+
+def attention_host_workspace_bytes(B, S, H, D, chunks=1, prologue=True, partial_dtype=torch.float32,
+                                   out_dtype=torch.bfloat16) -> int:
+    """Device workspace bytes dit_attention_host needs for these sizes."""
+    return int(load_library().dit_attention_host_workspace(B, S, H, D, chunks, int(bool(prologue)),
+                                                           _dtype_code(partial_dtype), _dtype_code(out_dtype)))
+
+
+def dit_attention_host(q, k, v, wq=None, wk=None, cos=None, sin=None, eps: float = 1e-6, chunks: int = 1,
+                       scale: float | None = None, partial_dtype=torch.float32, out_dtype=torch.bfloat16,
+                       prologue: bool = True, o=None, lse=None, workspace=None, stream=None):
+    """The whole hot path from host tensors (pinned for asynchronous copies): q, k, v bf16 [B, S, H, D]; wq, wk
+    fp32 [D]; cos, sin fp32 [S, D/2].  The value rows of each KV chunk are copied while earlier chunks compute.
+    Returns host (o, lse); they are valid once the stream has completed the call, and the inputs must stay
+    referenced until then (the copies read them asynchronously).  `workspace` is a device uint8 tensor of at
+    least attention_host_workspace_bytes(...) bytes (allocated here when None)."""
+    lib = load_library()
+    for t in (q, k, v):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 host tensors")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, S, H, D]")
+    B, S, H, D = q.shape
+    if prologue:
+        for t in (wq, wk, cos, sin):
+            if t is None or t.device.type != "cpu" or t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError("wq, wk, cos, sin must be contiguous fp32 host tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    pin = q.is_pinned()
+    if o is None:
+        o = torch.empty((B, S, H, D), dtype=out_dtype, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, pin_memory=pin)
+    if o.device.type != "cpu" or lse.device.type != "cpu" or not (o.is_contiguous() and lse.is_contiguous()):
+        raise ValueError("o and lse must be contiguous host tensors")
+    need = attention_host_workspace_bytes(B, S, H, D, chunks, prologue, partial_dtype, o.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+        if stream is not None:  # the allocator must not hand the block out again before `stream` is done with it
+            workspace.record_stream(stream)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a device tensor of at least {need} bytes")
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(lib.dit_attention_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(wq), ptr(wk), ptr(cos), ptr(sin),
+                                  B, S, H, D, float(eps), float(scale), int(chunks), int(bool(prologue)),
+                                  _dtype_code(partial_dtype), o.data_ptr(), _dtype_code(o.dtype), lse.data_ptr(),
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+    return o, lse
 
 
 def ring_overlap_attention(q, k_local, v_local, remote_kv, scale: float | None = None, out_dtype=torch.bfloat16,

@@ -12,6 +12,8 @@
  *                       result in its epilogue (the ring step's update_out_and_lse)
  *   dit_layer_norm_modulate, dit_rms_norm   row normalisations of the DiT block
  *   dit_quant_fp8_rows, dit_gemm_fp8        W8A8 fp8 projection
+ *   dit_attention_host  the whole hot path from host buffers, copies pipelined
+ *                       against the kernels
  *
  * Conventions shared by every entry point
  *   - Tensors are device pointers owned by the caller.  Activations are
@@ -34,6 +36,7 @@
 #ifndef DITATTN_H
 #define DITATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -276,6 +279,50 @@ dit_status dit_quant_fp8_rows(const void *x, void *codes, float *scale, int64_t 
  */
 dit_status dit_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,
                         int M, int N, int K, int64_t lda, int64_t ldb, int64_t ldo, struct CUstream_st *stream);
+
+/*
+ * dit_attention_host -- the whole hot path (prologue, attention over `chunks`
+ * equal KV chunks, LSE merge) on inputs in host memory, results back in host
+ * memory.
+ *
+ * Copies q, k (and, with the prologue, wq, wk, cos_tab, sin_tab) into the
+ * device workspace on an internal copy stream, then the value rows of each KV
+ * chunk in turn; on `stream` it runs dit_qk_norm_rope in place, dit_attn_fwd
+ * over chunk 0 (into a running result of partial_dtype, or straight into the
+ * output when chunks == 1) and dit_attn_fwd_update over every later chunk (the
+ * last one writing the output), each attention waiting only for its own value
+ * rows, and finally copies O and LSE to the host.  Chunk c covers keys
+ * [c*S/chunks, (c+1)*S/chunks).  Same operations and results as calling those
+ * entry points on device copies of the inputs.
+ *
+ * Defined by: the entry points it composes (see each); the chunk-by-chunk
+ * combination is the ring step of "feat: support Ascend NPU backend (torch_npu)
+ * for Qwen-Image pipelines - #274", item 2.
+ *
+ *   q, k, v          host bf16 [B, S, H, D], contiguous (pinned memory lets the
+ *                    copies run asynchronously); must stay valid until `stream`
+ *                    has passed this call
+ *   wq, wk           host fp32 [D]; cos_tab, sin_tab host fp32 [S, D/2]
+ *                    (ignored, may be NULL, when prologue == 0)
+ *   eps, scale       as for dit_qk_norm_rope / dit_attn_fwd
+ *   chunks           1 <= chunks <= S
+ *   prologue         1: QK-RMSNorm + RoPE first; 0: attention on q, k as given
+ *   partial_dtype    dtype of the running result between chunks
+ *   o, o_dtype       host [B, S, H, D] output; lse host fp32 [B, H, S]
+ *   workspace        device memory of at least dit_attention_host_workspace(...)
+ *                    bytes, 256-byte aligned, owned by the caller; it must not be
+ *                    used by other work until `stream` has passed this call
+ * Asynchronous on `stream`: o and lse are valid once `stream` has completed the
+ * call.  Errors as for the composed entry points; a workspace that is too small
+ * or misaligned is DIT_ERR_INVALID_ARG.
+ */
+size_t dit_attention_host_workspace(int B, int S, int H, int D, int chunks, int prologue,
+                                    dit_dtype partial_dtype, dit_dtype o_dtype);
+dit_status dit_attention_host(const void *q, const void *k, const void *v,
+                              const float *wq, const float *wk, const float *cos_tab, const float *sin_tab,
+                              int B, int S, int H, int D, float eps, float scale, int chunks, int prologue,
+                              dit_dtype partial_dtype, void *o, dit_dtype o_dtype, float *lse,
+                              void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
  * dit_poll_device_error -- synchronise `stream`, then read and clear the

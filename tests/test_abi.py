@@ -22,7 +22,7 @@ def lib():
 
 def _declared():
     text = HEADER.read_text()
-    return sorted(set(re.findall(r"^(?:const char \*|dit_status )(dit_\w+)\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:const char \*|dit_status |size_t )(dit_\w+)\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -194,3 +194,45 @@ def test_launch_overlap_setting(lib):
     assert lib.dit_set_launch_overlap(2) == ops.DIT_ERR_INVALID_ARG
     assert lib.dit_set_launch_overlap(0) == ops.DIT_OK
     assert lib.dit_set_launch_overlap(1) == ops.DIT_OK
+
+
+def _host(lib, **kw):
+    B, S, H, D = kw.pop("B", 1), kw.pop("S", 64), kw.pop("H", 2), kw.pop("D", 128)
+    chunks, prologue = kw.pop("chunks", 2), kw.pop("prologue", 1)
+    need = lib.dit_attention_host_workspace(B, S, H, D, chunks, 1, 1, 0)
+    a = dict(q=A16, k=A16 * 2, v=A16 * 3, wq=A16 * 4, wk=A16 * 5, cos=A16 * 6, sin=A16 * 7, o=A16 * 8, lse=A16 * 9,
+             ws=A16 * 16, wsb=need, pdt=1, odt=0)
+    a.update(kw)
+    return lib.dit_attention_host(a["q"], a["k"], a["v"], a["wq"], a["wk"], a["cos"], a["sin"], B, S, H, D, 1e-6,
+                                  0.088, chunks, prologue, a["pdt"], a["o"], a["odt"], a["lse"], a["ws"], a["wsb"],
+                                  None)
+
+
+def test_host_workspace_size(lib):
+    B, S, H, D = 2, 100, 3, 128
+    act = B * S * H * D * 2
+    n = lib.dit_attention_host_workspace(B, S, H, D, 2, 1, 1, 0)
+    # q, k, v, an fp32 running result, a bf16 output, LSE, tables: at least their sum
+    assert n >= 3 * act + 2 * act + act + B * H * S * 4 + 2 * S * (D // 2) * 4
+    assert lib.dit_attention_host_workspace(B, S, H, D, 1, 0, 1, 0) < n  # no running result, no tables
+    assert lib.dit_attention_host_workspace(B, S, H, D, 0, 1, 1, 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), ops.DIT_ERR_UNSUPPORTED),
+    (dict(chunks=0), ops.DIT_ERR_INVALID_ARG),
+    (dict(chunks=65), ops.DIT_ERR_INVALID_ARG),
+    (dict(prologue=2), ops.DIT_ERR_INVALID_ARG),
+    (dict(q=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(cos=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(ws=A16 * 16 + 128), ops.DIT_ERR_INVALID_ARG),   # workspace not 256-byte aligned
+    (dict(wsb=1024), ops.DIT_ERR_INVALID_ARG),            # workspace too small
+    (dict(pdt=5), ops.DIT_ERR_INVALID_ARG),
+])
+def test_host_path_rejects_bad_arguments(lib, kw, code):
+    assert _host(lib, **kw) == code
+    assert lib.dit_last_error_detail() != b""
+
+
+def test_host_path_empty_work_is_ok(lib):
+    assert _host(lib, B=0) == ops.DIT_OK

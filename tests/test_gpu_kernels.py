@@ -493,3 +493,55 @@ def test_w8a8_projection_accuracy():
     cos = float((out * ref).sum() / (np.linalg.norm(out) * np.linalg.norm(ref)))
     print(f"w8a8 relative error {rel:.4f}, cosine {cos:.6f}")
     assert rel < 0.06 and cos > 0.998
+
+
+# ---------------------------------------------------------------- the hot path from host buffers
+
+@pytest.mark.parametrize("B,S,H,D,chunks,prologue,pdt,odt,pinned", [
+    (1, 256, 2, 64, 4, True, "f32", "bf16", True),     # the tiny workload's shape
+    (2, 300, 3, 128, 3, True, "f32", "f32", True),     # B = 2: value rows of a chunk are strided copies
+    (2, 333, 2, 128, 2, False, "bf16", "bf16", False),  # no prologue, pageable host memory
+    (1, 129, 4, 64, 1, True, "f32", "bf16", True),     # one chunk: no running result
+])
+def test_attention_host_matches_device_path(orc, B, S, H, D, chunks, prologue, pdt, odt, pinned):
+    dts = {"bf16": torch.bfloat16, "f32": torch.float32}
+    q, k, v, wq, wk, cos, sin = inputs.small_case(B, S, H, D, seed=S + chunks)
+    host = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)  # noqa
+    hq, hk, hv = host(q), host(k), host(v)
+    hw = [torch.from_numpy(np.ascontiguousarray(t)) for t in (wq, wk, cos, sin)]
+    if pinned:
+        hq, hk, hv = hq.pin_memory(), hk.pin_memory(), hv.pin_memory()
+        hw = [t.pin_memory() for t in hw]
+    o, lse = ops.dit_attention_host(hq, hk, hv, *hw, eps=1e-6, chunks=chunks, partial_dtype=dts[pdt],
+                                    out_dtype=dts[odt], prologue=prologue)
+    torch.cuda.synchronize()  # (hq, hk, hv, hw stay referenced until here)
+    ops.poll_device_error()
+    od, ld = ops.dit_attention(dev_bf16(q), dev_bf16(k), dev_bf16(v), *(dev_f32(t) for t in (wq, wk, cos, sin)),
+                               eps=1e-6, chunks=chunks, partial_dtype=dts[pdt], out_dtype=dts[odt],
+                               prologue=prologue, merge="update")
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+    if not prologue:
+        ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
+        check_o(o.double().numpy(), ro, f32=odt == "f32", what="host path", vmax=vmax(v))
+        check_lse(lse.double().numpy(), rl, what="host path")
+
+
+def test_attention_host_back_to_back_calls_share_a_workspace():
+    """Two calls on one stream with one workspace and different inputs: the second call's copies wait for the
+    first call's kernels (the workspace is reused), so each result matches its own inputs."""
+    B, S, H, D = 1, 400, 2, 128
+    outs = []
+    ws = torch.empty(ops.attention_host_workspace_bytes(B, S, H, D, 2), dtype=torch.uint8, device="cuda")
+    cases = [inputs.small_case(B, S, H, D, seed=s) for s in (1, 2)]
+    host = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()  # noqa
+    keep = []  # the host inputs must outlive the asynchronous copies
+    for q, k, v, wq, wk, cos, sin in cases:
+        args = [host(q), host(k), host(v)] + [torch.from_numpy(np.ascontiguousarray(t)).pin_memory()
+                                              for t in (wq, wk, cos, sin)]
+        keep.append(args)
+        outs.append(ops.dit_attention_host(*args, chunks=2, workspace=ws))
+    torch.cuda.synchronize()
+    for (o, lse), (q, k, v, wq, wk, cos, sin) in zip(outs, cases):
+        od, ld = ops.dit_attention(dev_bf16(q), dev_bf16(k), dev_bf16(v),
+                                   *(dev_f32(t) for t in (wq, wk, cos, sin)), chunks=2, merge="update")
+        assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
