@@ -205,6 +205,7 @@ def config_of(w, chunks, args):
                                              else " (LSE-merge kernel)")) if chunks > 1 else "none",
             "prologue": w.prologue, "causal": False,
             "launch_overlap": not getattr(args, "no_launch_overlap", False),
+            "attention_variant": getattr(args, "attention_variant", 0),
             "scale": "1/sqrt(D)", "l2": "flushed before every timed step (512 MiB write)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
@@ -252,6 +253,7 @@ def run_ours(args):
     build.build()
     ops.load_library()
     ops.set_launch_overlap(not args.no_launch_overlap)
+    ops.set_attention_variant(args.attention_variant)
 
     inp = inputs.make_inputs(args.workload)
     w = inp.w
@@ -592,6 +594,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--chunks", type=int, default=0, help="KV chunks (0: the workload's own)")
+    ap.add_argument("--attention-variant", type=int, choices=[0, 1, 2], default=0,
+                    help="attention kernel for head dim 128: 0 default, 1 one CTA, 2 CTA pairs")
     ap.add_argument("--no-launch-overlap", action="store_true",
                     help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
     ap.add_argument("--merge", choices=["auto", "kernel", "update"], default="auto",

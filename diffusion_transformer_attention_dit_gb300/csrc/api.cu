@@ -14,6 +14,7 @@ namespace {
 
 thread_local const char *g_detail = "";
 std::atomic<int> g_launch_overlap{1};
+std::atomic<int> g_attention_variant{0};
 
 dit_status fail(dit_status s, const char *why) {
   g_detail = why;
@@ -43,8 +44,16 @@ dit_status from_cuda(cudaError_t e, const char *detail) {
 
 bool ditattn::launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
 void ditattn::set_error_detail(const char *why) { g_detail = why; }
+int ditattn::attention_variant() { return g_attention_variant.load(std::memory_order_relaxed); }
 
 extern "C" {
+
+dit_status dit_set_attention_variant(int variant) {
+  g_detail = "";
+  if (variant < 0 || variant > 2) return fail(DIT_ERR_INVALID_ARG, "variant must be 0, 1 or 2");
+  g_attention_variant.store(variant, std::memory_order_relaxed);
+  return DIT_OK;
+}
 
 dit_status dit_set_launch_overlap(int enable) {
   g_detail = "";
@@ -229,10 +238,11 @@ dit_status dit_poll_device_error(struct CUstream_st *stream) {
   if (e == cudaSuccess) e = ditattn::read_and_clear_attn_error(&va);
   if (e == cudaSuccess) e = ditattn::read_and_clear_prologue_error(&vp);
   if (e == cudaSuccess) e = ditattn::read_and_clear_merge_error(&vm);
-  unsigned int vf = 0;
+  unsigned int vf = 0, vq = 0;
   if (e == cudaSuccess) e = ditattn::read_and_clear_fp8_error(&vf);
+  if (e == cudaSuccess) e = ditattn::read_and_clear_pair_error(&vq);
   if (e != cudaSuccess) return from_cuda(e, nullptr);
-  if (va | vp | vm | vf) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (va | vp | vm | vf | vq) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return DIT_OK;
 }
 

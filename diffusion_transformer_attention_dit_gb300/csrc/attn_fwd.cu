@@ -42,6 +42,7 @@
 
 #include <mutex>
 
+#include "attn_math.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -50,6 +51,8 @@ namespace ditattn {
 __device__ unsigned int g_device_error = 0;
 
 namespace {
+
+using namespace attn;
 
 constexpr int kBM = 128;            // query rows per tile (MMA M)
 constexpr int kBN = 128;            // keys per block (MMA N of S, K of PV)
@@ -104,48 +107,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity) {
       return false;
     }
   }
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Packed pairs of fp32 (one 64-bit register pair) for the FFMA2 / FADD2 / FMUL2 pipes.
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_split(uint64_t v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
 }
 
 template <int D, bool kCausal, bool kUpdate>
@@ -620,6 +581,10 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
                             bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
                             bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
                             const char **detail) {
+  // D = 128, non-causal: CTA pairs when selected (variant 2)
+  if (D == 128 && !causal && attention_variant() == 2)
+    return launch_attn_fwd_pair(q, k, v, B, H, Sq, Skv, q_st, kv_st, scale, kv_begin, kv_end, o, o_f32, o_st, lse,
+                                o_acc, acc_f32, acc_st, lse_acc, stream, detail);
   (void)Skv;
   CUtensorMap tq, tk, tv, to, tacc;
   const int n_kv = kv_end - kv_begin;

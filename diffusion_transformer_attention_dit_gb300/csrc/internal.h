@@ -12,6 +12,9 @@ namespace ditattn {
 // preamble overlap the previous kernel's tail).  Set by dit_set_launch_overlap.
 bool launch_overlap_enabled();
 
+// Attention kernel choice for D = 128 non-causal launches: 0 auto, 1 one CTA, 2 CTA pairs.
+int attention_variant();
+
 // Set the text dit_last_error_detail returns (for entry points outside api.cu).
 void set_error_detail(const char *why);
 
@@ -31,6 +34,27 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// As launch_kernel, in clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_overlap_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Attention forward over keys [kv_begin, kv_end) (causal: query i sees keys j <= i).
 // Strides in elements {b, s, h}.  With o_acc non-null (update form) the result is
 // LSE-merged with the running (o_acc, lse_acc) before it is written.
@@ -39,6 +63,14 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
                             bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
                             bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
                             const char **detail);
+
+// The same on CTA pairs (cta_group::2): D = 128, non-causal only.
+cudaError_t launch_attn_fwd_pair(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv,
+                                 const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
+                                 void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
+                                 bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
+                                 const char **detail);
+cudaError_t read_and_clear_pair_error(unsigned int *value);
 
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,
                                 const float *wk, const float *cos_tab, const float *sin_tab, int B, int S, int H,

@@ -21,7 +21,8 @@ DIT_BF16, DIT_F32 = 0, 1
 EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_device_error",
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
-            "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace")
+            "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace",
+            "dit_set_attention_variant")
 
 _lib = None
 
@@ -59,6 +60,7 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
     lib.dit_set_launch_overlap.argtypes = [i32]
+    lib.dit_set_attention_variant.argtypes = [i32]
     lib.dit_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, vp,
                                        i32, vp, vp, ctypes.c_size_t, vp]
     lib.dit_attention_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
@@ -66,7 +68,7 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
                  "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap",
-                 "dit_attention_host"):
+                 "dit_attention_host", "dit_set_attention_variant"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -281,6 +283,11 @@ def set_launch_overlap(enable: bool):
     """Programmatic dependent launch for the library's kernels (default on): a kernel's launch overlaps the tail of
     the previous kernel on its stream; every kernel waits for that kernel before touching global memory."""
     _check(load_library().dit_set_launch_overlap(1 if enable else 0))
+
+
+def set_attention_variant(variant: int):
+    """Attention kernel for head dim 128 without a mask: 0 default, 1 one CTA, 2 CTA pairs (cta_group::2)."""
+    _check(load_library().dit_set_attention_variant(int(variant)))
 
 
 def selftest_wait_timeout(stream=None):

@@ -354,6 +354,16 @@ dit_status dit_selftest_wait_timeout(struct CUstream_st *stream);
  */
 dit_status dit_set_launch_overlap(int enable);
 
+/*
+ * dit_set_attention_variant -- which attention kernel serves head dim 128
+ * without a causal mask (dit_attn_fwd, dit_attn_fwd_update, dit_attention_host):
+ * 0 = the library's default, 1 = one CTA per 256 query rows, 2 = CTA pairs
+ * (clusters of 2 running M = 256 tcgen05 MMAs, each SM holding half of every
+ * K/V block).  Results agree to floating-point rounding; both are tested.
+ * Process-wide; DIT_ERR_INVALID_ARG for any other value.
+ */
+dit_status dit_set_attention_variant(int variant);
+
 /* dit_status_string -- static, human-readable name of a status code (never NULL). */
 const char *dit_status_string(dit_status s);
 

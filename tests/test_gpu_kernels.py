@@ -545,3 +545,69 @@ def test_attention_host_back_to_back_calls_share_a_workspace():
         od, ld = ops.dit_attention(dev_bf16(q), dev_bf16(k), dev_bf16(v),
                                    *(dev_f32(t) for t in (wq, wk, cos, sin)), chunks=2, merge="update")
         assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
+# ---------------------------------------------------------------- CTA-pair attention (cta_group::2)
+
+@pytest.fixture
+def pair_variant():
+    ops.set_attention_variant(2)
+    yield
+    ops.set_attention_variant(0)
+
+
+PAIR_SHAPES = [
+    # B, H, Sq, Skv: one pair; a partial second CTA; a pair with an empty second CTA; several pairs, ragged keys
+    (1, 2, 256, 256), (2, 3, 200, 333), (1, 1, 1, 1), (1, 1, 517, 3), (1, 2, 600, 1000), (2, 4, 1100, 700),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv", PAIR_SHAPES)
+@pytest.mark.parametrize("o_dtype", ["bf16", "f32"])
+def test_pair_attention_parity(orc, pair_variant, B, H, Sq, Skv, o_dtype):
+    q, k, v, *_ = inputs.small_case(B, Sq, H, 128, seed=3 * Sq + Skv, Skv=Skv)
+    dt = torch.bfloat16 if o_dtype == "bf16" else torch.float32
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    o, lse = ops.attn_fwd(tq, tk, tv, o_dtype=dt)
+    ops.poll_device_error()
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(128))
+    check_o(host_f64(o), ro, f32=o_dtype == "f32", what=f"pair {B, H, Sq, Skv}", vmax=vmax(v))
+    check_lse(host_f64(lse), rl, what=f"pair {B, H, Sq, Skv}")
+    ops.set_attention_variant(1)
+    o1, l1 = ops.attn_fwd(tq, tk, tv, o_dtype=dt)
+    check_o(host_f64(o), host_f64(o1), f32=o_dtype == "f32", what="pair vs one CTA", vmax=vmax(v))
+    check_lse(host_f64(lse), host_f64(l1), what="pair vs one CTA")
+
+
+def test_pair_chunks_update_and_rescale(orc, pair_variant):
+    """Key chunks, the update form (fp32 running O in place, then bf16), a sharp softmax (K x 8) and determinism."""
+    B, H, S = 1, 3, 1300
+    q, k, v, *_ = inputs.small_case(B, S, H, 128, seed=71, k_std=8.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+    for lo, hi in [(0, 64), (100, 333), (129, 1300)]:
+        o, lse = ops.attn_fwd(tq, tk, tv, None, lo, hi, o_dtype=torch.float32)
+        ro, rl = orc.attention(*f, 1 / math.sqrt(128), lo, hi)
+        check_o(host_f64(o), ro, f32=True, what=f"pair chunk [{lo},{hi})", vmax=vmax(v[:, lo:hi]))
+        check_lse(host_f64(lse), rl, what=f"pair chunk [{lo},{hi})")
+    edges = [0, 400, 800, 1300]
+    acc, lse = ops.attn_fwd(tq, tk, tv, None, edges[0], edges[1], o_dtype=torch.float32)
+    ops.attn_fwd_update(tq, tk, tv, acc, lse, None, edges[1], edges[2], o=acc, lse=lse)
+    o = torch.empty((B, S, H, 128), dtype=torch.bfloat16, device="cuda")
+    ops.attn_fwd_update(tq, tk, tv, acc, lse, None, edges[2], edges[3], o=o, lse=lse)
+    ops.poll_device_error()
+    ro, rl = orc.attention(*f, 1 / math.sqrt(128))
+    check_o(host_f64(o), ro, what="pair update chain")
+    check_lse(host_f64(lse), rl, what="pair update chain")
+    # a bf16 running O rounds the partial once more (the precision loss of bf16 ring partials), so it is
+    # checked on inputs with an ordinary softmax, as for the one-CTA kernel
+    q2, k2, v2, *_ = inputs.small_case(B, S, H, 128, seed=72, k_std=2.0)
+    tq2, tk2, tv2 = dev_bf16(q2), dev_bf16(k2), dev_bf16(v2)
+    acc_b, lse_b = ops.attn_fwd(tq2, tk2, tv2, None, 0, 650, o_dtype=torch.bfloat16)
+    o_b, l_b = ops.attn_fwd_update(tq2, tk2, tv2, acc_b, lse_b, None, 650, S)
+    ro2, rl2 = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q2, k2, v2)), 1 / math.sqrt(128))
+    check_o(host_f64(o_b), ro2, what="pair update, bf16 running O")
+    check_lse(host_f64(l_b), rl2, what="pair update, bf16 running O")
+    o2, l2 = ops.attn_fwd(tq, tk, tv)
+    o3, l3 = ops.attn_fwd(tq, tk, tv)
+    assert torch.equal(o2, o3) and torch.equal(l2, l3)
