@@ -12,7 +12,8 @@ namespace ditattn {
 // preamble overlap the previous kernel's tail).  Set by dit_set_launch_overlap.
 bool launch_overlap_enabled();
 
-// Attention kernel choice for D = 128 non-causal launches: 0 auto, 1 one CTA, 2 CTA pairs.
+// Attention kernel choice for D = 128 non-causal launches: 0 auto, 1 one CTA, 2 CTA pairs,
+// 3 CTA pairs with one tile per CTA and three S buffers.
 int attention_variant();
 
 // Set the text dit_last_error_detail returns (for entry points outside api.cu).
@@ -64,12 +65,13 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
                             bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
                             const char **detail);
 
-// The same on CTA pairs (cta_group::2): D = 128, non-causal only.
+// The same on CTA pairs (cta_group::2): D = 128, non-causal only.  one_tile: one
+// query tile per CTA with three S buffers; else two tiles per CTA.
 cudaError_t launch_attn_fwd_pair(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv,
                                  const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
                                  void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
-                                 bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
-                                 const char **detail);
+                                 bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool one_tile,
+                                 cudaStream_t stream, const char **detail);
 cudaError_t read_and_clear_pair_error(unsigned int *value);
 
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,

@@ -549,10 +549,11 @@ def test_attention_host_back_to_back_calls_share_a_workspace():
 
 # ---------------------------------------------------------------- CTA-pair attention (cta_group::2)
 
-@pytest.fixture
-def pair_variant():
-    ops.set_attention_variant(2)
-    yield
+@pytest.fixture(params=[2, 3], ids=["two_tiles", "one_tile_3S"])
+def pair_variant(request):
+    """The CTA-pair kernels: two query tiles per CTA, or one tile with three S buffers."""
+    ops.set_attention_variant(request.param)
+    yield request.param
     ops.set_attention_variant(0)
 
 
@@ -573,7 +574,7 @@ def test_pair_attention_parity(orc, pair_variant, B, H, Sq, Skv, o_dtype):
     ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(128))
     check_o(host_f64(o), ro, f32=o_dtype == "f32", what=f"pair {B, H, Sq, Skv}", vmax=vmax(v))
     check_lse(host_f64(lse), rl, what=f"pair {B, H, Sq, Skv}")
-    ops.set_attention_variant(1)
+    ops.set_attention_variant(1)  # (the fixture restores the default)
     o1, l1 = ops.attn_fwd(tq, tk, tv, o_dtype=dt)
     check_o(host_f64(o), host_f64(o1), f32=o_dtype == "f32", what="pair vs one CTA", vmax=vmax(v))
     check_lse(host_f64(lse), host_f64(l1), what="pair vs one CTA")

@@ -38,9 +38,10 @@ def _device_compare(a: torch.Tensor, b: torch.Tensor):
 @pytest.mark.parametrize("name,merge,variant", [("qwen_image", "update", 0), ("qwen_image", "kernel", 0),
                                                 ("qwen_image_edit", "update", 0), ("wan480", "kernel", 0),
                                                 ("wan720", "kernel", 0), ("qwen_image", "update", 2),
-                                                ("wan480", "kernel", 2)])
+                                                ("wan480", "kernel", 2), ("qwen_image", "update", 3),
+                                                ("wan480", "kernel", 3)])
 def test_workload_parity(name, merge, variant):
-    """variant: the attention kernel for head dim 128 (0 the default, 2 CTA pairs)."""
+    """variant: the attention kernel for head dim 128 (0 the default, 2 and 3 the CTA-pair kernels)."""
     ops.set_attention_variant(variant)
     try:
         _workload_parity(name, merge)
