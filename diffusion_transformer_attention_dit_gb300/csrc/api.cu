@@ -50,7 +50,7 @@ extern "C" {
 
 dit_status dit_set_attention_variant(int variant) {
   g_detail = "";
-  if (variant < 0 || variant > 3) return fail(DIT_ERR_INVALID_ARG, "variant must be 0, 1, 2 or 3");
+  if (variant < 0 || variant > 3) return fail(DIT_ERR_INVALID_ARG, "variant must be 0 to 3");
   g_attention_variant.store(variant, std::memory_order_relaxed);
   return DIT_OK;
 }

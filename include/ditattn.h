@@ -359,7 +359,9 @@ dit_status dit_set_launch_overlap(int enable);
  * without a causal mask (dit_attn_fwd, dit_attn_fwd_update, dit_attention_host):
  * 0 = the library's default, 1 = one CTA per 256 query rows, 2 = CTA pairs
  * (clusters of 2 running M = 256 tcgen05 MMAs, each SM holding half of every
- * K/V block).  Results agree to floating-point rounding; both are tested.
+ * K/V block), 3 = CTA pairs with one query tile per CTA and S computed three
+ * blocks ahead.  Variants 2 and 3 serve only the non-causal calls (causal ones
+ * use the default).  Results agree to floating-point rounding; all are tested.
  * Process-wide; DIT_ERR_INVALID_ARG for any other value.
  */
 dit_status dit_set_attention_variant(int variant);

@@ -236,3 +236,10 @@ def test_host_path_rejects_bad_arguments(lib, kw, code):
 
 def test_host_path_empty_work_is_ok(lib):
     assert _host(lib, B=0) == ops.DIT_OK
+
+
+def test_attention_variant_setting(lib):
+    assert lib.dit_set_attention_variant(4) == ops.DIT_ERR_INVALID_ARG
+    assert lib.dit_set_attention_variant(-1) == ops.DIT_ERR_INVALID_ARG
+    for v in (3, 2, 1, 0):
+        assert lib.dit_set_attention_variant(v) == ops.DIT_OK

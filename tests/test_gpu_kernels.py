@@ -549,7 +549,7 @@ def test_attention_host_back_to_back_calls_share_a_workspace():
 
 # ---------------------------------------------------------------- CTA-pair attention (cta_group::2)
 
-@pytest.fixture(params=[2, 3], ids=["two_tiles", "one_tile_3S"])
+@pytest.fixture(params=[2, 3], ids=["pair_two_tiles", "pair_one_tile_3S"])
 def pair_variant(request):
     """The CTA-pair kernels: two query tiles per CTA, or one tile with three S buffers."""
     ops.set_attention_variant(request.param)
@@ -612,3 +612,4 @@ def test_pair_chunks_update_and_rescale(orc, pair_variant):
     o2, l2 = ops.attn_fwd(tq, tk, tv)
     o3, l3 = ops.attn_fwd(tq, tk, tv)
     assert torch.equal(o2, o3) and torch.equal(l2, l3)
+
