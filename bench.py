@@ -594,9 +594,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--chunks", type=int, default=0, help="KV chunks (0: the workload's own)")
-    ap.add_argument("--attention-variant", type=int, choices=[0, 1, 2, 3], default=0,
-                    help="attention kernel for head dim 128: 0 default, 1 one CTA, 2 CTA pairs with two tiles per "
-                         "CTA, 3 CTA pairs with one tile per CTA and three S buffers")
+    ap.add_argument("--attention-variant", type=int, choices=[0, 1, 2, 3, 4], default=0,
+                    help="attention kernel for head dim 128: 0 default, 1 one CTA (P in TMEM), 2 CTA pairs with two "
+                         "tiles per CTA, 3 CTA pairs with one tile per CTA and three S buffers, 4 one CTA with P in "
+                         "shared memory")
     ap.add_argument("--no-launch-overlap", action="store_true",
                     help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
     ap.add_argument("--merge", choices=["auto", "kernel", "update"], default="auto",

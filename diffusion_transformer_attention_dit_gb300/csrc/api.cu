@@ -50,7 +50,7 @@ extern "C" {
 
 dit_status dit_set_attention_variant(int variant) {
   g_detail = "";
-  if (variant < 0 || variant > 3) return fail(DIT_ERR_INVALID_ARG, "variant must be 0 to 3");
+  if (variant < 0 || variant > 4) return fail(DIT_ERR_INVALID_ARG, "variant must be 0 to 4");
   g_attention_variant.store(variant, std::memory_order_relaxed);
   return DIT_OK;
 }
@@ -238,11 +238,12 @@ dit_status dit_poll_device_error(struct CUstream_st *stream) {
   if (e == cudaSuccess) e = ditattn::read_and_clear_attn_error(&va);
   if (e == cudaSuccess) e = ditattn::read_and_clear_prologue_error(&vp);
   if (e == cudaSuccess) e = ditattn::read_and_clear_merge_error(&vm);
-  unsigned int vf = 0, vq = 0;
+  unsigned int vf = 0, vq = 0, vs = 0;
   if (e == cudaSuccess) e = ditattn::read_and_clear_fp8_error(&vf);
   if (e == cudaSuccess) e = ditattn::read_and_clear_pair_error(&vq);
+  if (e == cudaSuccess) e = ditattn::read_and_clear_ps_error(&vs);
   if (e != cudaSuccess) return from_cuda(e, nullptr);
-  if (va | vp | vm | vf | vq) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (va | vp | vm | vf | vq | vs) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return DIT_OK;
 }
 

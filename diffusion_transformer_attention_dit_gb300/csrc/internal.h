@@ -12,8 +12,8 @@ namespace ditattn {
 // preamble overlap the previous kernel's tail).  Set by dit_set_launch_overlap.
 bool launch_overlap_enabled();
 
-// Attention kernel choice for D = 128 non-causal launches: 0 auto, 1 one CTA, 2 CTA pairs,
-// 3 CTA pairs with one tile per CTA and three S buffers.
+// Attention kernel choice for D = 128 launches: 0 auto, 1 one CTA (P in TMEM), 2 CTA pairs, 3 CTA pairs
+// with one tile per CTA and three S buffers (2 and 3 non-causal only), 4 one CTA with P in shared memory.
 int attention_variant();
 
 // Set the text dit_last_error_detail returns (for entry points outside api.cu).
@@ -73,6 +73,14 @@ cudaError_t launch_attn_fwd_pair(const void *q, const void *k, const void *v, in
                                  bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool one_tile,
                                  cudaStream_t stream, const char **detail);
 cudaError_t read_and_clear_pair_error(unsigned int *value);
+
+// The same with P in shared memory (S of the next block overlaps the softmax): D = 128.
+cudaError_t launch_attn_fwd_ps(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv,
+                               const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
+                               bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
+                               bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
+                               const char **detail);
+cudaError_t read_and_clear_ps_error(unsigned int *value);
 
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,
                                 const float *wk, const float *cos_tab, const float *sin_tab, int B, int S, int H,

@@ -360,8 +360,10 @@ dit_status dit_set_launch_overlap(int enable);
  * 0 = the library's default, 1 = one CTA per 256 query rows, 2 = CTA pairs
  * (clusters of 2 running M = 256 tcgen05 MMAs, each SM holding half of every
  * K/V block), 3 = CTA pairs with one query tile per CTA and S computed three
- * blocks ahead.  Variants 2 and 3 serve only the non-causal calls (causal ones
- * use the default).  Results agree to floating-point rounding; all are tested.
+ * blocks ahead, 4 = one CTA per 256 rows with P kept in shared memory (S of the
+ * next block computed while the softmax runs; also serves causal calls).
+ * Variants 2 and 3 serve only the non-causal calls (causal ones use the
+ * default).  Results agree to floating-point rounding; all are tested.
  * Process-wide; DIT_ERR_INVALID_ARG for any other value.
  */
 dit_status dit_set_attention_variant(int variant);

@@ -239,7 +239,7 @@ def test_host_path_empty_work_is_ok(lib):
 
 
 def test_attention_variant_setting(lib):
-    assert lib.dit_set_attention_variant(4) == ops.DIT_ERR_INVALID_ARG
+    assert lib.dit_set_attention_variant(5) == ops.DIT_ERR_INVALID_ARG
     assert lib.dit_set_attention_variant(-1) == ops.DIT_ERR_INVALID_ARG
-    for v in (3, 2, 1, 0):
+    for v in (4, 3, 2, 1, 0):
         assert lib.dit_set_attention_variant(v) == ops.DIT_OK

@@ -549,9 +549,10 @@ def test_attention_host_back_to_back_calls_share_a_workspace():
 
 # ---------------------------------------------------------------- CTA-pair attention (cta_group::2)
 
-@pytest.fixture(params=[2, 3], ids=["pair_two_tiles", "pair_one_tile_3S"])
+@pytest.fixture(params=[2, 3, 4], ids=["pair_two_tiles", "pair_one_tile_3S", "p_in_smem"])
 def pair_variant(request):
-    """The CTA-pair kernels: two query tiles per CTA, or one tile with three S buffers."""
+    """The alternative head-dim-128 kernels: CTA pairs with two query tiles per CTA, CTA pairs with one tile and
+    three S buffers, one CTA with P in shared memory."""
     ops.set_attention_variant(request.param)
     yield request.param
     ops.set_attention_variant(0)
@@ -613,3 +614,67 @@ def test_pair_chunks_update_and_rescale(orc, pair_variant):
     o3, l3 = ops.attn_fwd(tq, tk, tv)
     assert torch.equal(o2, o3) and torch.equal(l2, l3)
 
+
+
+# ---------------------------------------------------------------- sizes at the edges
+
+def test_attn_long_sequence_sampled_rows(orc):
+    """131072 queries and keys (one head): 512 CTAs along the rows and 1024 key blocks per CTA, so every ring
+    and S/P barrier goes through hundreds of phases; sampled rows (first, last, ragged tail, random) vs the
+    oracle over all keys, plain and update forms."""
+    from parity import sample_rows
+    B, H, S, D = 1, 1, 131072, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=2024)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    o, lse = ops.attn_fwd(tq, tk, tv)
+    acc, lse_acc = ops.attn_fwd(tq, tk, tv, None, 0, 70001, o_dtype=torch.float32)
+    o2, l2 = ops.attn_fwd_update(tq, tk, tv, acc, lse_acc, None, 70001, S)
+    ops.poll_device_error()
+    rows = sample_rows(S, 16, seed=5)
+    rt = torch.from_numpy(rows).cuda()
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D), rows=rows)
+    for got_o, got_l, what in [(o, lse, "long"), (o2, l2, "long, update form")]:
+        check_o(host_f64(got_o.index_select(1, rt)), ro, what=what)
+        check_lse(host_f64(got_l.index_select(2, rt)), rl, what=what)
+
+
+def test_empty_inputs_launch_nothing():
+    """Zero-sized work through the binding returns empty results without a launch or an error."""
+    e = torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    o, lse = ops.attn_fwd(e, e, e)
+    assert o.shape == (1, 0, 2, 128) and lse.shape == (1, 2, 0)
+    o, lse = ops.attn_merge_lse(torch.empty((2, 1, 0, 2, 128), device="cuda"),
+                                torch.empty((2, 1, 2, 0), device="cuda"))
+    assert o.numel() == 0 and lse.numel() == 0
+    w = torch.ones(128, device="cuda")
+    tab = torch.empty((0, 64), device="cuda")
+    qo, ko = ops.qk_norm_rope(e, e, w, w, tab, tab)
+    assert qo.numel() == 0 and ko.numel() == 0
+    x = torch.empty((0, 5120), dtype=torch.bfloat16, device="cuda")
+    assert ops.rms_norm(x, torch.ones(5120, device="cuda")).numel() == 0
+    codes, scale = ops.quant_fp8_rows(x)
+    assert codes.numel() == 0 and scale.numel() == 0
+    ops.poll_device_error()
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv", [(1, 2, 256, 256), (2, 3, 200, 333), (1, 1, 517, 300), (1, 2, 700, 700)])
+def test_p_in_smem_causal(orc, B, H, Sq, Skv):
+    """The P-in-shared-memory kernel behind the causal entry point, and causal chunks in both orders merged by
+    the update form (rows that see nothing in one part take the other part)."""
+    ops.set_attention_variant(4)
+    try:
+        q, k, v, *_ = inputs.small_case(B, Sq, H, 128, seed=Sq + 7 * Skv, Skv=Skv, k_std=2.0)
+        tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+        f = [inputs.bf16_bits_to_f64(x) for x in (q, k, v)]
+        o, lse = ops.attn_fwd(tq, tk, tv, o_dtype=torch.float32, causal=True)
+        ops.poll_device_error()
+        ro, rl = orc.attention(*f, 1 / math.sqrt(128), causal=True)
+        check_o(host_f64(o), ro, f32=True, what=f"p-in-smem causal {B, H, Sq, Skv}", vmax=vmax(v))
+        check_lse(host_f64(lse), rl, what=f"p-in-smem causal {B, H, Sq, Skv}")
+        cut = Skv // 3
+        acc, lse_acc = ops.attn_fwd(tq, tk, tv, None, cut, Skv, o_dtype=torch.float32, causal=True)
+        o2, l2 = ops.attn_fwd_update(tq, tk, tv, acc, lse_acc, None, 0, cut, o_dtype=torch.float32, causal=True)
+        check_o(host_f64(o2), ro, f32=True, what="p-in-smem causal update", vmax=vmax(v))
+        check_lse(host_f64(l2), rl, what="p-in-smem causal update")
+    finally:
+        ops.set_attention_variant(0)

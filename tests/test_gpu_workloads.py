@@ -39,9 +39,11 @@ def _device_compare(a: torch.Tensor, b: torch.Tensor):
                                                 ("qwen_image_edit", "update", 0), ("wan480", "kernel", 0),
                                                 ("wan720", "kernel", 0), ("qwen_image", "update", 2),
                                                 ("wan480", "kernel", 2), ("qwen_image", "update", 3),
-                                                ("wan480", "kernel", 3)])
+                                                ("wan480", "kernel", 3), ("qwen_image", "update", 4),
+                                                ("wan480", "kernel", 4), ("wan720", "kernel", 4)])
 def test_workload_parity(name, merge, variant):
-    """variant: the attention kernel for head dim 128 (0 the default, 2 and 3 the CTA-pair kernels)."""
+    """variant: the attention kernel for head dim 128 (0 the default, 2 and 3 the CTA-pair kernels, 4 P in
+    shared memory)."""
     ops.set_attention_variant(variant)
     try:
         _workload_parity(name, merge)
