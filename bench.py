@@ -45,8 +45,8 @@ MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", 
 # DRAM bytes (read + write) of the attention launches of one bench step, from an ncu capture
 # (profiles/launch_list_qwen_image_step.md): chunk 0 (fp32 running O) and chunk 1 (update form,
 # bf16 O), averaged per launch; valid for the attention source it was taken on.
-ATTN_TRAFFIC = {"source_sha256_prefix": "c160fd6dea2d0dd5",
-                "qwen_image": ((28.04 + 53.96) + (97.32 + 59.13)) / 2 * 1e6}
+ATTN_TRAFFIC = {"source_sha256_prefix": "8398519fcb136921",
+                "qwen_image": ((29.79 + 56.26) + (98.23 + 58.58)) / 2 * 1e6}
 
 
 def peaks():
