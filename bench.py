@@ -36,6 +36,7 @@ METRIC = "attention TFLOP/s (4·B·H·Sq·Skv·D/t) and % of GB300 dense bf16 pe
 FALLBACK_TFLOPS = 1900.0
 FALLBACK_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
+ATTN_TIMED_STEPS = 1000  # steps of the separate attention-timing region (roofline.achieved)
 PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480": "f32", "wan720": "bf16"}
 # How the KV chunks are combined: "update" folds each later chunk into the running (O, LSE) in its attention
 # epilogue; "kernel" writes stacked per-chunk partials and runs the LSE-merge kernel (Wan720's workload
@@ -45,8 +46,8 @@ MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", 
 # DRAM bytes (read + write) of the attention launches of one bench step, from an ncu capture
 # (profiles/launch_list_qwen_image_step.md): chunk 0 (fp32 running O) and chunk 1 (update form,
 # bf16 O), averaged per launch; valid for the attention source it was taken on.
-ATTN_TRAFFIC = {"source_sha256_prefix": "8398519fcb136921",
-                "qwen_image": ((29.79 + 56.26) + (98.23 + 58.58)) / 2 * 1e6}
+ATTN_TRAFFIC = {"source_sha256_prefix": "5f5d8b30479990a5",
+                "qwen_image": ((30.54 + 56.23) + (97.52 + 58.01)) / 2 * 1e6}
 
 
 def peaks():
@@ -269,48 +270,22 @@ def run_ours(args):
     q, k, v = (to_dev(host[n].view(np.int16)) for n in ("q", "k", "v"))
     wq, wk, cos, sin = (torch.from_numpy(a).to(dev) for a in (inp.wq, inp.wk, inp.cos, inp.sin))
     B, S, H, D = w.B, w.S, w.H, w.D
-    qn, kn = torch.empty_like(q), torch.empty_like(k)
-    o_parts = torch.empty((chunks, B, S, H, D), dtype=pdt, device=dev)
-    lse_parts = torch.empty((chunks, B, H, S), dtype=torch.float32, device=dev)
     o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    bounds = w.chunk_bounds(chunks)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     merge = merge_mode(w, args)
     launches_per_step = (1 if w.prologue else 0) + chunks + (1 if chunks > 1 and merge == "kernel" else 0)
+    # one C call per step (dit_attention): prologue into the workspace, the KV chunks (chunk c covers keys
+    # [c*S/chunks, (c+1)*S/chunks)), then the merge -- in the update form in the last chunk's epilogue, else by
+    # the merge kernel over stacked partials.  The events bracket the attention launches alone.
+    ws = torch.empty(max(1, ops.attention_workspace_bytes(B, S, H, D, chunks, w.prologue, pdt, merge)),
+                     dtype=torch.uint8, device=dev)
 
     def step(attn_events=None):
-        if w.prologue:
-            ops.qk_norm_rope(q, k, wq, wk, cos, sin, w.eps, q_out=qn, k_out=kn)
-            aq, ak = qn, kn
-        else:
-            aq, ak = q, k
-        if chunks == 1:
-            if attn_events is not None:
-                attn_events[0].record(stream)
-            ops.attn_fwd(aq, ak, v, None, 0, S, o=o, lse=lse)
-            if attn_events is not None:
-                attn_events[1].record(stream)
-            return
-        if attn_events is not None:
-            attn_events[0].record(stream)
-        if merge == "update":
-            # chunk 0 starts the running result; later chunks merge into it in their epilogues, the last one
-            # straight into the bf16 output
-            ops.attn_fwd(aq, ak, v, None, *bounds[0], o=o_parts[0], lse=lse)
-            for lo, hi in bounds[1:-1]:
-                ops.attn_fwd_update(aq, ak, v, o_parts[0], lse, None, lo, hi, o=o_parts[0], lse=lse)
-            ops.attn_fwd_update(aq, ak, v, o_parts[0], lse, None, *bounds[-1], o=o, lse=lse)
-            if attn_events is not None:
-                attn_events[1].record(stream)
-            return
-        for c, (lo, hi) in enumerate(bounds):
-            ops.attn_fwd(aq, ak, v, None, lo, hi, o=o_parts[c], lse=lse_parts[c])
-        if attn_events is not None:
-            attn_events[1].record(stream)
-        ops.attn_merge_lse(o_parts, lse_parts, o=o, lse=lse)
+        ops.dit_attention(q, k, v, wq, wk, cos, sin, eps=w.eps, chunks=chunks, partial_dtype=pdt,
+                          prologue=w.prologue, merge=merge, o=o, lse=lse, workspace=ws, attn_events=attn_events)
 
     for _ in range(args.warmup):
         step()
@@ -330,27 +305,43 @@ def run_ours(args):
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:  # noqa: BLE001
         pass
-    step_ms, attn_ms = [], []
+    def made(n):  # events created (recorded once) before a timed region, so none is created inside it
+        evs = [ev() for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    # Timed region: whole steps only.  Events between the kernels of a step stall the stream and cut the launch
+    # overlap between them (about 11 us per Qwen-Image step), so the step region carries none; the attention
+    # launches are timed in a second region of the same steps below.
+    step_ev = made(2 * args.steps)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with ClockSampler(uuid) as clocks:
-        for _ in range(args.steps):
+        for i in range(args.steps):
             flush.zero_()
-            e0, e1, a0, a1 = ev(), ev(), ev(), ev()
-            e0.record(stream)
-            step((a0, a1))
-            e1.record(stream)
-            step_ms.append((e0, e1))
-            attn_ms.append((a0, a1))
+            step_ev[2 * i].record(stream)
+            step()
+            step_ev[2 * i + 1].record(stream)
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     ops.poll_device_error()
-    t_steps = sum(a.elapsed_time(b) for a, b in step_ms) / 1e3
-    t_attn = sum(a.elapsed_time(b) for a, b in attn_ms) / 1e3
+    t_steps = sum(step_ev[2 * i].elapsed_time(step_ev[2 * i + 1]) for i in range(args.steps)) / 1e3
+    # Attention region: the same steps with events recorded (by dit_attention, on this stream) right before the
+    # first and after the last attention launch; achieved = attention flops / the time between them.
+    attn_steps = min(args.steps, ATTN_TIMED_STEPS)
+    attn_ev = made(2 * attn_steps)
+    torch.cuda.synchronize()
+    for i in range(attn_steps):
+        flush.zero_()
+        step((attn_ev[2 * i], attn_ev[2 * i + 1]))
+    torch.cuda.synchronize()
+    ops.poll_device_error()
+    t_attn = sum(attn_ev[2 * i].elapsed_time(attn_ev[2 * i + 1]) for i in range(attn_steps)) / 1e3
     flops_step = w.attention_flops()
     t_max, value = aggregate(t_steps, flops_step, args.steps, world, dev)
 
@@ -403,7 +394,7 @@ def run_ours(args):
 
     if rank == 0:
         peak_tf, peak_gbs, src = peaks()
-        achieved = flops_step * args.steps / t_attn / 1e12
+        achieved = flops_step * attn_steps / t_attn / 1e12
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
@@ -411,7 +402,9 @@ def run_ours(args):
             "config": config_of(w, chunks, args),
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved, "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": achieved / peak_tf, "peak_source": src,
-                         "traffic": args.traffic if args.traffic is not None else attn_traffic(w.name)},
+                         "traffic": args.traffic if args.traffic is not None else attn_traffic(w.name),
+                         "timing": f"{attn_steps} further steps with events right before the first and after the "
+                                   "last attention launch (the step region carries no events between kernels)"},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "api": "dit_attention_host (copies pipelined per KV chunk)" if host_path
                     else "torch copies + ops.dit_attention"},

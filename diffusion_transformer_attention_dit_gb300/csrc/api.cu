@@ -111,7 +111,7 @@ dit_status attn_common(const void *q, const void *k, const void *v, int B, int H
                        bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
                        struct CUstream_st *stream, bool update = false, const void *o_acc = nullptr,
                        dit_dtype acc_dtype = DIT_BF16, const int64_t acc_strides[3] = nullptr,
-                       const float *lse_acc = nullptr) {
+                       const float *lse_acc = nullptr, bool defer_wait = false) {
   g_detail = "";
   if (B < 0 || H < 0 || Sq < 0 || Skv < 0) return fail(DIT_ERR_INVALID_ARG, "negative size");
   if (D != 64 && D != 128) return fail(DIT_ERR_UNSUPPORTED, "head dim must be 64 or 128");
@@ -164,12 +164,22 @@ dit_status attn_common(const void *q, const void *k, const void *v, int B, int H
   const char *detail = nullptr;
   cudaError_t e = ditattn::launch_attn_fwd(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end,
                                            causal, o, o_dtype == DIT_F32, o_strides, lse, update ? o_acc : nullptr,
-                                           acc_dtype == DIT_F32, acc_strides, lse_acc,
+                                           acc_dtype == DIT_F32, acc_strides, lse_acc, defer_wait,
                                            reinterpret_cast<cudaStream_t>(stream), &detail);
   return from_cuda(e, detail);
 }
 
 }  // namespace
+
+dit_status ditattn::attn_checked(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                                 const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
+                                 int kv_end, bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3],
+                                 float *lse, const void *o_acc, dit_dtype acc_dtype, const int64_t acc_strides[3],
+                                 const float *lse_acc, bool defer_wait, cudaStream_t stream) {
+  return attn_common(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end, causal, o, o_dtype,
+                     o_strides, lse, reinterpret_cast<struct CUstream_st *>(stream), o_acc != nullptr, o_acc,
+                     acc_dtype, acc_strides, lse_acc, defer_wait);
+}
 
 extern "C" {
 

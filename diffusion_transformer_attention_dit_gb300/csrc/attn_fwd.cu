@@ -34,6 +34,15 @@
 // Every mbarrier wait is bounded (about 2 s); a wait that gives up sets the
 // library's device error word and the CTA drains its in-flight copies and MMAs,
 // frees TMEM and exits.
+//
+// Deferred dependency wait (a later chunk of one attention, launched right
+// after the previous chunk on the same stream): Q, K and V were complete before
+// the previous chunk started, so the kernel starts its blocks at once, beside
+// the previous launch's last wave, and calls griddepcontrol.wait only where it
+// needs that launch's results -- the update form before it loads O_acc (TMA
+// producer) and reads LSE_acc (epilogue threads), the plain form before its
+// CTAs exit.  Either way no CTA ends before the previous launch has, so the
+// launches still complete in stream order.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -92,6 +101,7 @@ struct AttnArgs {
   float *lse;
   const float *lse_acc;  // update form: running LSE [B, H, Sq] (may equal lse)
   int acc_f32;           // update form: O_acc is fp32 (else bf16)
+  int defer_wait;        // wait for the previous launch only where its results are needed (see above)
 };
 
 // Bounded wait; false (and the device error word set) if the phase did not complete in time.
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Update form: the O_acc tile of query tile t, half hf, is ring fill 2 * nblk + hf * kNQ + t
   // (one 128 x D bf16 tile, or two halves of an fp32 tile, per ring slot).
   const int acc_halves = kUpdate ? (args.acc_f32 ? 2 : 1) : 0;
-  griddep_wait();
+  if (!args.defer_wait) griddep_wait();
   griddep_launch_dependents();
 
   const uint32_t bars = base + L::kBar;
@@ -198,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++issued;
         }
       }
+      if (kUpdate && args.defer_wait) griddep_wait();  // O_acc is the previous launch's output
       // Update form: the O_acc tiles follow the last K/V block through the ring.
       // A slot holds D / 64 boxes of 128 rows x 128 bytes: a whole bf16 tile, or
       // half of an fp32 tile (boxes of 32 columns).
@@ -392,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float wc = l > 0.f ? 1.0f / l : 0.f, wa = 0.f;
       float lse_out = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
       if (kUpdate) {
+        if (args.defer_wait) griddep_wait();  // LSE_acc is the previous launch's output
         // base 2: this range's LSE is m + log2 l; O_c = acc / l, so its weight
         // e^(LSE_c - L) / l is 2^(m - L2)
         const int q = tile_q0 + row;
@@ -504,6 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // plain form, deferred: the CTA may not end before the previous launch has
+  if (!kUpdate && args.defer_wait && threadIdx.x == 0) griddep_wait();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -579,9 +593,10 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
 cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                             const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
                             bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
-                            bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
-                            const char **detail) {
-  // D = 128: P in shared memory (variant 4), or non-causal CTA pairs (variants 2, 3)
+                            bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool defer_wait,
+                            cudaStream_t stream, const char **detail) {
+  // D = 128: P in shared memory (variant 4), or non-causal CTA pairs (variants 2, 3); those
+  // kernels always wait for the previous launch at their start (defer_wait is a hint)
   if (D == 128 && attention_variant() == 4)
     return launch_attn_fwd_ps(q, k, v, B, H, Sq, Skv, q_st, kv_st, scale, kv_begin, kv_end, causal, o, o_f32, o_st,
                               lse, o_acc, acc_f32, acc_st, lse_acc, stream, detail);
@@ -618,6 +633,7 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
   a.lse = lse;
   a.lse_acc = lse_acc;
   a.acc_f32 = acc_f32 ? 1 : 0;
+  a.defer_wait = defer_wait ? 1 : 0;
   if (update) {
     if (causal)
       return D == 64 ? launch_typed<64, true, true>(tq, tk, tv, to, tacc, a, B, stream)

@@ -8,8 +8,9 @@
 //   caller stream:            prologue (waits q, k) | attention chunk 0 (waits its v rows) |
 //                             chunk 1 in the update form (waits its v rows) | ... | O, LSE to the host
 // so the value rows of later chunks travel while earlier chunks compute.  The
-// attention kernels are the ones behind dit_attn_fwd / dit_attn_fwd_update and
-// the prologue is dit_qk_norm_rope; chunk c covers keys [c*S/C, (c+1)*S/C).
+// attention kernels are the ones behind dit_attn_fwd / dit_attn_fwd_update, in
+// the chunk sequence dit_attention uses (attention_path.cu), and the prologue is
+// dit_qk_norm_rope; chunk c covers keys [c*S/C, (c+1)*S/C).
 
 #include <cuda_runtime.h>
 
@@ -163,22 +164,20 @@ dit_status dit_attention_host(const void *q, const void *k, const void *v, const
                           reinterpret_cast<const float *>(ws + L.wk), reinterpret_cast<const float *>(ws + L.cs),
                           reinterpret_cast<const float *>(ws + L.sn), B, S, H, D, eps, stream_);
   if (st != DIT_OK) return st;  // the entry point has set the detail
-  const int64_t strides[3] = {(int64_t)S * H * D, (int64_t)H * D, D};
   float *dlse = reinterpret_cast<float *>(ws + L.lse);
-  for (int c = 0; c < chunks; ++c) {
-    const int lo = (int)((int64_t)c * S / chunks), hi = (int)((int64_t)(c + 1) * S / chunks);
-    if (!ok(cudaStreamWaitEvent(stream, evs.ev[2 + c], 0))) return host_fail(DIT_ERR_CUDA, cudaGetErrorString(e));
-    const bool last = c == chunks - 1;
-    void *out = last ? ws + L.o : ws + L.acc;
-    const dit_dtype out_dt = last ? o_dtype : partial_dtype;
-    if (c == 0)
-      st = dit_attn_fwd(dq, dk, dv, B, H, S, S, D, strides, strides, scale, lo, hi, out, out_dt, strides, dlse,
-                        stream_);
-    else
-      st = dit_attn_fwd_update(dq, dk, dv, B, H, S, S, D, strides, strides, scale, lo, hi, 0, ws + L.acc,
-                               partial_dtype, strides, dlse, out, out_dt, strides, dlse, stream_);
-    if (st != DIT_OK) return st;
-  }
+  // chunk c waits only for its own value rows (copy event 2 + c)
+  struct Ctx {
+    cudaStream_t stream;
+    cudaEvent_t *ev;
+  } ctx = {stream, evs.ev.data()};
+  auto before_chunk = [](void *p, int c) -> cudaError_t {
+    const Ctx *x = static_cast<const Ctx *>(p);
+    return cudaStreamWaitEvent(x->stream, x->ev[2 + c], 0);
+  };
+  st = ditattn::run_attention_chunks(dq, dk, dv, B, S, H, D, scale, chunks, partial_dtype, true,
+                                     chunks > 1 ? ws + L.acc : nullptr, nullptr, ws + L.o, o_dtype, dlse, nullptr,
+                                     nullptr, before_chunk, &ctx, stream);
+  if (st != DIT_OK) return st;
   const size_t o_bytes = (size_t)B * S * H * D * (o_dtype == DIT_F32 ? 4 : 2);
   ok(cudaMemcpyAsync(o, ws + L.o, o_bytes, cudaMemcpyDeviceToHost, stream)) &&
       ok(cudaMemcpyAsync(lse, dlse, (size_t)B * H * S * 4, cudaMemcpyDeviceToHost, stream));

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/ditattn.h"
+
 namespace ditattn {
 
 // Whether launches carry programmatic stream serialisation (each kernel calls
@@ -58,12 +60,15 @@ cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
 
 // Attention forward over keys [kv_begin, kv_end) (causal: query i sees keys j <= i).
 // Strides in elements {b, s, h}.  With o_acc non-null (update form) the result is
-// LSE-merged with the running (o_acc, lse_acc) before it is written.
+// LSE-merged with the running (o_acc, lse_acc) before it is written.  defer_wait:
+// the previous launch on the stream is the previous chunk of the same attention
+// (it writes only what this launch reads as o_acc / lse_acc, or nothing this
+// launch touches), so the dependency wait moves to where its results are needed.
 cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                             const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
                             bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
-                            bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
-                            const char **detail);
+                            bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool defer_wait,
+                            cudaStream_t stream, const char **detail);
 
 // The same on CTA pairs (cta_group::2): D = 128, non-causal only.  one_tile: one
 // query tile per CTA with three S buffers; else two tiles per CTA.
@@ -116,5 +121,30 @@ cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
 cudaError_t read_and_clear_attn_error(unsigned int *value);
 cudaError_t read_and_clear_prologue_error(unsigned int *value);
 cudaError_t read_and_clear_merge_error(unsigned int *value);
+
+// The attention entry points' argument checks, then launch_attn_fwd (api.cu).
+// o_acc == nullptr: plain form; otherwise the update form.  defer_wait as above.
+dit_status attn_checked(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
+                        const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin, int kv_end,
+                        bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
+                        const void *o_acc, dit_dtype acc_dtype, const int64_t acc_strides[3], const float *lse_acc,
+                        bool defer_wait, cudaStream_t stream);
+
+// Attention over `chunks` equal KV chunks of contiguous bf16 BSHD q, k, v
+// (chunk c = keys [c*S/chunks, (c+1)*S/chunks)) and their merge, on `stream`
+// (attention_path.cu).  merge_update: chunk 0 writes the running result `acc`
+// (partial_dtype, BSHD), every later chunk is merged into it in its epilogue
+// (dit_attn_fwd_update), the last one straight into o.  Otherwise chunk c
+// writes part c of the stacked `acc` [chunks, B, S, H, D] and lse_parts
+// [chunks, B, H, S], and dit_attn_merge_lse combines them.  chunks == 1 writes
+// o and lse directly.  Chunks after the first defer their dependency wait.
+// attn_begin / attn_end (may be null) are recorded before the first and after
+// the last attention launch.  before_chunk (may be null) runs on the host
+// before chunk c is launched (the host path makes the stream wait there for
+// that chunk's value rows).
+dit_status run_attention_chunks(const void *q, const void *k, const void *v, int B, int S, int H, int D, float scale,
+                                int chunks, dit_dtype partial_dtype, bool merge_update, void *acc, float *lse_parts,
+                                void *o, dit_dtype o_dtype, float *lse, cudaEvent_t attn_begin, cudaEvent_t attn_end,
+                                cudaError_t (*before_chunk)(void *ctx, int c), void *ctx, cudaStream_t stream);
 
 }  // namespace ditattn

@@ -22,7 +22,7 @@ EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
             "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace",
-            "dit_set_attention_variant")
+            "dit_set_attention_variant", "dit_attention", "dit_attention_workspace")
 
 _lib = None
 
@@ -65,10 +65,14 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
                                        i32, vp, vp, ctypes.c_size_t, vp]
     lib.dit_attention_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.dit_attention_host_workspace.restype = ctypes.c_size_t
+    lib.dit_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, i32, vp,
+                                  i32, vp, vp, ctypes.c_size_t, vp, vp, vp]
+    lib.dit_attention_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.dit_attention_workspace.restype = ctypes.c_size_t
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
                  "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap",
-                 "dit_attention_host", "dit_set_attention_variant"):
+                 "dit_attention_host", "dit_set_attention_variant", "dit_attention"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -295,34 +299,70 @@ def selftest_wait_timeout(stream=None):
     _check(load_library().dit_selftest_wait_timeout(_stream(stream)))
 
 
+def attention_workspace_bytes(B, S, H, D, chunks=1, prologue=True, partial_dtype=torch.float32,
+                              merge: str = "kernel") -> int:
+    """Device workspace bytes dit_attention needs for these sizes."""
+    return int(load_library().dit_attention_workspace(B, S, H, D, chunks, int(bool(prologue)),
+                                                      _dtype_code(partial_dtype), int(merge == "update")))
+
+
+def _event_handle(ev, stream) -> int:
+    # torch creates the CUDA event on its first record: record a fresh one once so the handle exists (the library
+    # records it again at the right place on the stream); create events ahead of a timed region to avoid that
+    if ev is None:
+        return 0
+    if not ev.cuda_event:
+        ev.record(stream)
+    return ev.cuda_event
+
+
 def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1, scale: float | None = None,
                   partial_dtype=torch.float32, out_dtype=torch.bfloat16, prologue: bool = True, stream=None,
-                  merge: str = "kernel"):
-    """The whole hot path: prologue, attention over `chunks` KV chunks, LSE merge.  Returns (o, lse).
+                  merge: str = "kernel", o=None, lse=None, workspace=None, attn_events=None):
+    """The whole hot path in one C call (dit_attention): prologue, attention over `chunks` KV chunks, merge.
+    Returns (o, lse).
 
     merge="kernel": every chunk writes (O_c, LSE_c) into stacked partials and one merge kernel combines them.
     merge="update": chunk 0 writes a running result (partial_dtype), every later chunk is LSE-merged into it in
-    its attention epilogue, the last one straight into the output."""
-    B, S, H, D = q.shape
-    Skv = k.shape[1]
-    if prologue:
-        q, k = qk_norm_rope(q, k, wq, wk, cos, sin, eps, stream=stream)
-    if chunks == 1:
-        return attn_fwd(q, k, v, scale, o_dtype=out_dtype, stream=stream)
-    edges = [(i * Skv) // chunks for i in range(chunks + 1)]
-    if merge == "update":
-        acc, lse = attn_fwd(q, k, v, scale, edges[0], edges[1], o_dtype=partial_dtype, stream=stream)
-        for c in range(1, chunks - 1):
-            attn_fwd_update(q, k, v, acc, lse, scale, edges[c], edges[c + 1], o=acc, lse=lse, stream=stream)
-        o = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
-        return attn_fwd_update(q, k, v, acc, lse, scale, edges[-2], edges[-1], o=o, lse=lse, stream=stream)
-    if merge != "kernel":
+    its attention epilogue, the last one straight into the output.  `workspace`: a device uint8 tensor of at least
+    attention_workspace_bytes(...) bytes (allocated here when None).  attn_events: optional pair of
+    torch.cuda.Event recorded before the first and after the last attention launch."""
+    if merge not in ("kernel", "update"):
         raise ValueError("merge must be 'kernel' or 'update'")
-    o_parts = torch.empty((chunks, B, S, H, D), dtype=partial_dtype, device=q.device)
-    lse_parts = torch.empty((chunks, B, H, S), dtype=torch.float32, device=q.device)
-    for c in range(chunks):
-        attn_fwd(q, k, v, scale, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c], stream=stream)
-    return attn_merge_lse(o_parts, lse_parts, out_dtype=out_dtype, stream=stream)
+    lib = load_library()
+    _cuda(q, k, v)
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 [B, S, H, D] tensors")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same shape [B, S, H, D]")
+    B, S, H, D = q.shape
+    if prologue:
+        _cuda(wq, wk, cos, sin)
+        for t in (wq, wk, cos, sin):
+            if t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError("wq, wk, cos, sin must be contiguous fp32 tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if o is None:
+        o = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    _cuda(o, lse)
+    if not o.is_contiguous() or not lse.is_contiguous() or lse.dtype != torch.float32:
+        raise ValueError("o must be contiguous; lse contiguous fp32")
+    need = attention_workspace_bytes(B, S, H, D, chunks, prologue, partial_dtype, merge)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _cuda(workspace)
+    st = torch.cuda.current_stream() if stream is None else stream
+    e0, e1 = (None, None) if attn_events is None else attn_events
+    ptr = (lambda t: t.data_ptr()) if prologue else (lambda t: None)
+    _check(lib.dit_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(wq), ptr(wk), ptr(cos), ptr(sin), B, S, H,
+                             D, eps, scale, chunks, int(bool(prologue)), _dtype_code(partial_dtype),
+                             int(merge == "update"), o.data_ptr(), _dtype_code(o.dtype), lse.data_ptr(),
+                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                             _event_handle(e0, st), _event_handle(e1, st), st.cuda_stream))
+    return o, lse
 
 
 def attention_host_workspace_bytes(B, S, H, D, chunks=1, prologue=True, partial_dtype=torch.float32,

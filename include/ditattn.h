@@ -12,6 +12,7 @@
  *                       result in its epilogue (the ring step's update_out_and_lse)
  *   dit_layer_norm_modulate, dit_rms_norm   row normalisations of the DiT block
  *   dit_quant_fp8_rows, dit_gemm_fp8        W8A8 fp8 projection
+ *   dit_attention       the whole hot path on device buffers, one call
  *   dit_attention_host  the whole hot path from host buffers, copies pipelined
  *                       against the kernels
  *
@@ -44,6 +45,7 @@ extern "C" {
 #endif
 
 struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+struct CUevent_st;  /* cudaEvent_t is `struct CUevent_st *` */
 
 typedef enum {
     DIT_OK = 0,
@@ -323,6 +325,55 @@ dit_status dit_attention_host(const void *q, const void *k, const void *v,
                               int B, int S, int H, int D, float eps, float scale, int chunks, int prologue,
                               dit_dtype partial_dtype, void *o, dit_dtype o_dtype, float *lse,
                               void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
+ * dit_attention -- the whole hot path (prologue, attention over `chunks` equal
+ * KV chunks, LSE merge) on device buffers, in one call.
+ *
+ * Runs dit_qk_norm_rope (into the workspace), then the attention over chunk c
+ * = keys [c*S/chunks, (c+1)*S/chunks) for every c, then the merge: with
+ * merge_update = 1, dit_attn_fwd over chunk 0 into a running result of
+ * partial_dtype and dit_attn_fwd_update over every later chunk (the last one
+ * writing o); with merge_update = 0, dit_attn_fwd of every chunk into stacked
+ * partials of partial_dtype and dit_attn_merge_lse.  chunks == 1 writes o and
+ * lse directly.  Same operations and bit-identical results as calling those
+ * entry points in that order.  Chunks after the first are launched so that
+ * they start beside the previous chunk's last wave and wait for it only where
+ * they read its results (update form) or before they end (stacked partials);
+ * launches still complete in stream order.
+ *
+ * Defined by: the entry points it composes; the chunk-by-chunk combination is
+ * the ring step of "feat: support Ascend NPU backend (torch_npu) for Qwen-Image
+ * pipelines - #274", item 2, and the stacked merge the LSE merge of its
+ * sequence-parallel paths.
+ *
+ *   q, k, v          device bf16 [B, S, H, D], contiguous; not modified
+ *   wq, wk           device fp32 [D]; cos_tab, sin_tab device fp32 [S, D/2]
+ *                    (ignored, may be NULL, when prologue == 0)
+ *   eps, scale       as for dit_qk_norm_rope / dit_attn_fwd
+ *   chunks           1 <= chunks <= S; merge_update 0 or 1 (ignored for 1 chunk)
+ *   partial_dtype    dtype of the running result / stacked partials
+ *   o, o_dtype       device [B, S, H, D] output, contiguous; lse device fp32
+ *                    [B, H, S]
+ *   workspace        device memory of at least dit_attention_workspace(...)
+ *                    bytes, 256-byte aligned, owned by the caller and not
+ *                    overlapping any argument; it must not be used by other
+ *                    work until `stream` has passed this call (may be NULL when
+ *                    that size is 0)
+ *   attn_begin, attn_end  events recorded on `stream` before the first and
+ *                    after the last attention launch (for timing the attention
+ *                    alone); either may be NULL
+ * Errors as for the composed entry points; a workspace that is too small,
+ * misaligned or overlapping is DIT_ERR_INVALID_ARG.
+ */
+size_t dit_attention_workspace(int B, int S, int H, int D, int chunks, int prologue, dit_dtype partial_dtype,
+                               int merge_update);
+dit_status dit_attention(const void *q, const void *k, const void *v,
+                         const float *wq, const float *wk, const float *cos_tab, const float *sin_tab,
+                         int B, int S, int H, int D, float eps, float scale, int chunks, int prologue,
+                         dit_dtype partial_dtype, int merge_update, void *o, dit_dtype o_dtype, float *lse,
+                         void *workspace, size_t workspace_bytes, struct CUevent_st *attn_begin,
+                         struct CUevent_st *attn_end, struct CUstream_st *stream);
 
 /*
  * dit_poll_device_error -- synchronise `stream`, then read and clear the

@@ -243,3 +243,53 @@ def test_attention_variant_setting(lib):
     assert lib.dit_set_attention_variant(-1) == ops.DIT_ERR_INVALID_ARG
     for v in (4, 3, 2, 1, 0):
         assert lib.dit_set_attention_variant(v) == ops.DIT_OK
+
+
+def _device_path(lib, **kw):
+    B, S, H, D = kw.pop("B", 1), kw.pop("S", 64), kw.pop("H", 2), kw.pop("D", 128)
+    chunks, prologue, merge_update = kw.pop("chunks", 2), kw.pop("prologue", 1), kw.pop("merge_update", 1)
+    need = lib.dit_attention_workspace(B, S, H, D, chunks, 1, 1, 0)
+    a = dict(q=A16, k=A16 * 2, v=A16 * 3, wq=A16 * 4, wk=A16 * 5, cos=A16 * 6, sin=A16 * 7, o=A16 * 8, lse=A16 * 9,
+             ws=A16 * 16, wsb=need, pdt=1, odt=0)
+    a.update(kw)
+    return lib.dit_attention(a["q"], a["k"], a["v"], a["wq"], a["wk"], a["cos"], a["sin"], B, S, H, D, 1e-6, 0.088,
+                             chunks, prologue, a["pdt"], merge_update, a["o"], a["odt"], a["lse"], a["ws"], a["wsb"],
+                             None, None, None)
+
+
+def test_device_path_workspace_size(lib):
+    B, S, H, D, C = 2, 100, 3, 128, 4
+    act, lse = B * S * H * D, B * H * S * 4
+    # prologue outputs (bf16 q, k) + an fp32 running result; stacked partials and LSE for the merge kernel
+    upd = lib.dit_attention_workspace(B, S, H, D, C, 1, 1, 1)
+    assert upd >= 2 * act * 2 + act * 4
+    ker = lib.dit_attention_workspace(B, S, H, D, C, 1, 1, 0)
+    assert ker >= 2 * act * 2 + C * (act * 4 + lse)
+    assert lib.dit_attention_workspace(B, S, H, D, 1, 0, 1, 0) == 0   # one chunk, no prologue: nothing
+    assert lib.dit_attention_workspace(B, S, H, D, 1, 1, 1, 0) >= 2 * act * 2
+    assert lib.dit_attention_workspace(B, S, H, D, 0, 1, 1, 0) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), ops.DIT_ERR_UNSUPPORTED),
+    (dict(chunks=0), ops.DIT_ERR_INVALID_ARG),
+    (dict(chunks=65), ops.DIT_ERR_INVALID_ARG),
+    (dict(prologue=2), ops.DIT_ERR_INVALID_ARG),
+    (dict(merge_update=2), ops.DIT_ERR_INVALID_ARG),
+    (dict(q=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(cos=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(ws=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(ws=A16 * 16 + 128), ops.DIT_ERR_INVALID_ARG),   # workspace not 256-byte aligned
+    (dict(wsb=1024), ops.DIT_ERR_INVALID_ARG),            # workspace too small
+    (dict(ws=A16 * 8), ops.DIT_ERR_INVALID_ARG),          # workspace overlaps the output
+    (dict(pdt=5), ops.DIT_ERR_INVALID_ARG),
+    (dict(odt=7), ops.DIT_ERR_INVALID_ARG),
+])
+def test_device_path_rejects_bad_arguments(lib, kw, code):
+    assert _device_path(lib, **kw) == code
+    assert lib.dit_last_error_detail() != b""
+
+
+def test_device_path_empty_work_is_ok(lib):
+    assert _device_path(lib, B=0) == ops.DIT_OK
+    assert _device_path(lib, S=0, chunks=1) == ops.DIT_OK

@@ -547,6 +547,61 @@ def test_attention_host_back_to_back_calls_share_a_workspace():
         assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
 
 
+@pytest.mark.parametrize("merge,chunks,prologue,pdt", [
+    ("update", 2, True, "f32"), ("update", 3, False, "bf16"), ("update", 5, True, "bf16"),
+    ("kernel", 3, True, "f32"), ("kernel", 4, False, "bf16"), ("kernel", 1, True, "f32"),
+])
+def test_dit_attention_equals_its_entry_points(merge, chunks, prologue, pdt):
+    """The one-call path (later chunks start beside the previous chunk's last wave and wait for it only where they
+    need its results) is bit-identical to the same entry points called one by one, each waiting at its start."""
+    dts = {"bf16": torch.bfloat16, "f32": torch.float32}
+    B, S, H, D = 2, 1000, 4, 128
+    q, k, v, wq, wk, cos, sin = inputs.small_case(B, S, H, D, seed=chunks * 7 + len(merge))
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    tw = [dev_f32(t) for t in (wq, wk, cos, sin)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    o, lse = ops.dit_attention(tq, tk, tv, *tw, eps=1e-6, chunks=chunks, partial_dtype=dts[pdt], prologue=prologue,
+                               merge=merge, attn_events=(e0, e1))
+    aq, ak = ops.qk_norm_rope(tq, tk, *tw, 1e-6) if prologue else (tq, tk)
+    edges = [(i * S) // chunks for i in range(chunks + 1)]
+    if chunks == 1:
+        ro, rl = ops.attn_fwd(aq, ak, tv, None, 0, S)
+    elif merge == "update":
+        acc, rl = ops.attn_fwd(aq, ak, tv, None, edges[0], edges[1], o_dtype=dts[pdt])
+        for c in range(1, chunks - 1):
+            ops.attn_fwd_update(aq, ak, tv, acc, rl, None, edges[c], edges[c + 1], o=acc, lse=rl)
+        ro = torch.empty((B, S, H, D), dtype=torch.bfloat16, device="cuda")
+        ops.attn_fwd_update(aq, ak, tv, acc, rl, None, edges[-2], edges[-1], o=ro, lse=rl)
+    else:
+        parts = torch.empty((chunks, B, S, H, D), dtype=dts[pdt], device="cuda")
+        lparts = torch.empty((chunks, B, H, S), dtype=torch.float32, device="cuda")
+        for c in range(chunks):
+            ops.attn_fwd(aq, ak, tv, None, edges[c], edges[c + 1], o=parts[c], lse=lparts[c])
+        ro, rl = ops.attn_merge_lse(parts, lparts)
+    torch.cuda.synchronize()
+    ops.poll_device_error()
+    assert torch.equal(o, ro) and torch.equal(lse, rl)
+    assert e0.elapsed_time(e1) > 0.0
+
+
+def test_dit_attention_back_to_back_steps_share_a_workspace():
+    """Steps issued back to back on one stream with one workspace and different inputs (the next step's prologue
+    rewrites the workspace the previous step's last chunk reads): each result matches its own inputs."""
+    B, S, H, D = 1, 900, 3, 128
+    cases = [inputs.small_case(B, S, H, D, seed=s) for s in (3, 4, 5)]
+    dev = [[dev_bf16(q), dev_bf16(k), dev_bf16(v)] + [dev_f32(t) for t in (wq, wk, cos, sin)]
+           for q, k, v, wq, wk, cos, sin in cases]
+    for merge in ("update", "kernel"):
+        ws = torch.empty(ops.attention_workspace_bytes(B, S, H, D, 3, True, torch.float32, merge),
+                         dtype=torch.uint8, device="cuda")
+        outs = [ops.dit_attention(*args, chunks=3, merge=merge, workspace=ws) for args in dev]
+        torch.cuda.synchronize()
+        for (o, lse), args in zip(outs, dev):
+            ro, rl = ops.dit_attention(*args, chunks=3, merge=merge)
+            torch.cuda.synchronize()
+            assert torch.equal(o, ro) and torch.equal(lse, rl)
+
+
 # ---------------------------------------------------------------- CTA-pair attention (cta_group::2)
 
 @pytest.fixture(params=[2, 3, 4], ids=["pair_two_tiles", "pair_one_tile_3S", "p_in_smem"])
