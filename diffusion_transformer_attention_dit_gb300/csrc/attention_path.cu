@@ -116,6 +116,8 @@ dit_status dit_attention(const void *q, const void *k, const void *v, const floa
     return fail(DIT_ERR_INVALID_ARG, "unknown dtype");
   if ((int64_t)B * S * H == 0) return DIT_OK;
   if (chunks < 1 || chunks > S) return fail(DIT_ERR_INVALID_ARG, "chunks must satisfy 1 <= chunks <= S");
+  if (chunks > 1 && !merge_update && !ditattn::merge_fits(chunks, H))
+    return fail(DIT_ERR_UNSUPPORTED, "chunks * H too large for the merge kernel");
   if (!q || !k || !v || !o || !lse) return fail(DIT_ERR_INVALID_ARG, "null pointer");
   if (prologue && (!wq || !wk || !cos_tab || !sin_tab)) return fail(DIT_ERR_INVALID_ARG, "null pointer");
   const DeviceWs L = plan(B, S, H, D, chunks, prologue, partial_dtype, merge_update);

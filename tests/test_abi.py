@@ -293,3 +293,9 @@ def test_device_path_rejects_bad_arguments(lib, kw, code):
 def test_device_path_empty_work_is_ok(lib):
     assert _device_path(lib, B=0) == ops.DIT_OK
     assert _device_path(lib, S=0, chunks=1) == ops.DIT_OK
+
+
+def test_device_path_checks_the_merge_before_launching(lib):
+    # more stacked partials than the merge kernel takes: refused before anything is launched
+    assert _device_path(lib, S=2048, chunks=1100, merge_update=0, wsb=1 << 40) == ops.DIT_ERR_UNSUPPORTED
+    assert b"merge" in lib.dit_last_error_detail()
