@@ -22,7 +22,7 @@ EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
             "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace",
-            "dit_set_attention_variant", "dit_attention", "dit_attention_workspace")
+            "dit_set_attention_variant", "dit_attention", "dit_attention_workspace", "dit_attention_noalloc")
 
 _lib = None
 
@@ -69,10 +69,12 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
                                   i32, vp, vp, ctypes.c_size_t, vp, vp, vp]
     lib.dit_attention_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.dit_attention_workspace.restype = ctypes.c_size_t
+    lib.dit_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, i32,
+                                          vp, i32, vp, vp]
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
                  "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap",
-                 "dit_attention_host", "dit_set_attention_variant", "dit_attention"):
+                 "dit_attention_host", "dit_set_attention_variant", "dit_attention", "dit_attention_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p

@@ -376,6 +376,35 @@ dit_status dit_attention(const void *q, const void *k, const void *v,
                          struct CUevent_st *attn_end, struct CUstream_st *stream);
 
 /*
+ * dit_attention_noalloc -- dit_attention for callers that cannot allocate
+ * device memory: the same prologue, chunked attention and merge, with the
+ * workspace taken from a scratch array built into the library instead of one
+ * the caller provides.  For code that may not or cannot call cudaMalloc: a
+ * host callback, a plugin that a host framework hands only its input and
+ * output buffers, a process whose device memory budget belongs to someone
+ * else.
+ *
+ * The pages have no counterpart: this is a deployment convenience of this
+ * library, not part of the method.
+ *
+ *   arguments        as for dit_attention, without workspace and events
+ *   limit            the scratch holds 32 MiB: sizes whose
+ *                    dit_attention_workspace(...) is larger are refused with
+ *                    DIT_ERR_UNSUPPORTED before anything is launched
+ * The first call on a device brings the 32 MiB scratch onto that device (the
+ * CUDA runtime loads a library's device data on first use) and looks up its
+ * device address, with that device current; the memory stays reserved until
+ * the process exits.  Make that first call before any stream capture.  All calls share the scratch: nothing in it needs to start at
+ * zero, but calls that run concurrently on the GPU (other streams, other host
+ * threads) race on it.  Allocates nothing.  Errors as for dit_attention.
+ */
+dit_status dit_attention_noalloc(const void *q, const void *k, const void *v,
+                                 const float *wq, const float *wk, const float *cos_tab, const float *sin_tab,
+                                 int B, int S, int H, int D, float eps, float scale, int chunks, int prologue,
+                                 dit_dtype partial_dtype, int merge_update, void *o, dit_dtype o_dtype, float *lse,
+                                 struct CUstream_st *stream);
+
+/*
  * dit_poll_device_error -- synchronise `stream`, then read and clear the
  * library's device error word.  Returns DIT_OK, DIT_ERR_TIMEOUT if a bounded
  * device-side wait gave up since the last poll, or DIT_ERR_CUDA if the
