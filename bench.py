@@ -1,11 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark of the DiT attention hot path on GB300.
 
-One step = the whole path on one batch of synthetic input, resident in HBM:
-QK-RMSNorm + interleaved RoPE on Q and K, flash attention over the workload's
-KV chunks (each chunk writes O_c and LSE_c), and the LSE merge.  Default
+One step = the whole path on one batch of synthetic input, resident in HBM,
+as one dit_attention call: QK-RMSNorm + interleaved RoPE on Q and K, flash
+attention over the workload's KV chunks, and the LSE merge (in the last
+chunk's epilogue, or by the merge kernel over stacked partials).  Default
 workload: Qwen-Image joint attention (B1 H24 D128 S4312 = 256 text + 78x52
 image tokens), KV in 2 chunks.
+
+Timing: the step region records events around whole steps only (events
+between a step's kernels would stall the stream); roofline.achieved comes
+from a second region of the same steps whose events bracket the attention
+launches; e2e runs the public host-buffer call with the copies inside the
+timed region.
 
 Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
 (the only reference this method has) on a bounded sample of the same workload.
