@@ -2,20 +2,29 @@
 """Benchmark of the DiT attention hot path on GB300.
 
 One step = the whole path on one batch of synthetic input, resident in HBM,
-as one dit_attention call: QK-RMSNorm + interleaved RoPE on Q and K, flash
-attention over the workload's KV chunks, and the LSE merge (in the last
-chunk's epilogue, or by the merge kernel over stacked partials).  Default
-workload: Qwen-Image joint attention (B1 H24 D128 S4312 = 256 text + 78x52
-image tokens), KV in 2 chunks.
+as one dit_attention call: QK-RMSNorm + interleaved RoPE on Q and K (when the
+workload has it), flash attention over the workload's KV chunks, and the LSE
+merge (by the merge kernel over stacked partials, or in the last chunk's
+epilogue).  Default workload: Wan2.2 720p (B1 H40 D128 S75600 = 21x45x80
+patches, K x 3, no prologue), KV in 8 chunks with bf16 partials merged by the
+LSE-merge kernel.
 
-Timing: the step region records events around whole steps only (events
-between a step's kernels would stall the stream); roofline.achieved comes
-from a second region of the same steps whose events bracket the attention
-launches; e2e runs the public host-buffer call with the copies inside the
-timed region.
+The JSON line (rank 0) carries, beside the step throughput:
+  roofline      the attention launches of the step, timed in a second region of
+                the same steps (events around the attention launches only)
+  hbm           the step's merge kernel (events around it in that region) and
+                the QK-RMSNorm + RoPE prologue at the workload's shapes, timed
+                alone; algorithmic bytes / time against the measured HBM copy
+                bandwidth
+  per_workload  the other full-size workloads (Qwen-Image, Qwen-Image-Edit,
+                Wan2.2 480p), each its own step and attention regions
+  e2e           the public host-buffer call (dit_attention_host) with the
+                host<->device copies inside the timed region
+Every timed region has its own nvidia-smi clock record, holding only the
+samples taken while that region ran.
 
-Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
-(the only reference this method has) on a bounded sample of the same workload.
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 """
@@ -40,21 +49,20 @@ sys.path.insert(0, str(ROOT))
 from diffusion_transformer_attention_dit_gb300 import inputs  # noqa: E402
 
 METRIC = "attention TFLOP/s (4·B·H·Sq·Skv·D/t) and % of GB300 dense bf16 peak"
-FALLBACK_TFLOPS = 1900.0
-FALLBACK_GBS = 6800.0
+FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_FLUSH_BYTES = 512 << 20
-ATTN_TIMED_STEPS = 1000  # steps of the separate attention-timing region (roofline.achieved)
+REGION_S = 1.5           # target length of the regions whose step count bench.py chooses
+SAMPLER_WARMUP_S = 0.6   # nvidia-smi is given this long to start before a timed region
 PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480": "f32", "wan720": "bf16"}
 # How the KV chunks are combined: "update" folds each later chunk into the running (O, LSE) in its attention
 # epilogue; "kernel" writes stacked per-chunk partials and runs the LSE-merge kernel (Wan720's workload
 # specifies per-chunk bf16 partials merged by the merge kernel).
 MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", "wan480": "kernel",
          "wan720": "kernel"}
-# DRAM bytes (read + write) of the attention launches of one bench step, from an ncu capture
-# (profiles/launch_list_qwen_image_step.md): chunk 0 (fp32 running O) and chunk 1 (update form,
-# bf16 O), averaged per launch; valid for the attention source it was taken on.
-ATTN_TRAFFIC = {"source_sha256_prefix": "5f5d8b30479990a5",
-                "qwen_image": ((30.54 + 56.23) + (97.52 + 58.01)) / 2 * 1e6}
+PER_WORKLOAD = ("qwen_image", "qwen_image_edit", "wan480")
+# DRAM bytes (read + write) per attention launch, from an ncu capture of the attention source with this sha256
+# prefix; reported as roofline.traffic only while the source is unchanged.
+ATTN_TRAFFIC = {"source_sha256_prefix": None, "by_workload": {}, "capture": ""}
 
 
 def peaks():
@@ -62,31 +70,33 @@ def peaks():
     if path.exists():
         try:
             d = json.loads(path.read_text())
-            tf = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
-            gbs = d.get("hbm_gbs") or d.get("hbm_GBs")
-            if tf and gbs:
-                return float(tf), float(gbs), "measured"
-        except (ValueError, OSError):
+            out = {k: float(d[k]) for k in FALLBACK if d.get(k)}
+            if len(out) == len(FALLBACK):
+                return out, "measured"
+        except (ValueError, OSError, TypeError):
             pass
-    return FALLBACK_TFLOPS, FALLBACK_GBS, "fallback"
+    return dict(FALLBACK), "fallback"
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) taken while the timed region runs."""
+    """nvidia-smi samples (every 200 ms), each stamped with the host time it arrived; summary() keeps those that
+    arrived inside a given window (the timed region, plus one sampling period for the sample in flight)."""
 
     FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.2
 
     def __init__(self, uuid: str | None):
         self.uuid = uuid
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                          "-lms", str(int(self.PERIOD_S * 1000))], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except OSError:
             self.proc = None
@@ -94,7 +104,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def ready(self, timeout_s: float = SAMPLER_WARMUP_S):
+        """Wait (bounded) for the first sample, so the region's first samples are not lost to start-up."""
+        t0 = time.perf_counter()
+        while self.proc and not self.lines and time.perf_counter() - t0 < timeout_s:
+            time.sleep(0.02)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -104,12 +120,16 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        rows = [l.split(", ") for l in self.lines if l]
+    def summary(self, t0: float | None = None, t1: float | None = None):
+        rows = []
+        for t, line in self.lines:
+            if not line or (t0 is not None and t < t0) or (t1 is not None and t > t1 + self.PERIOD_S):
+                continue
+            rows.append(line.split(", "))
         if self.uuid:
             mine = [r for r in rows if r and self.uuid in r[0]]
             rows = mine or rows
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
@@ -117,32 +137,54 @@ class ClockSampler:
                 smax.append(float(r[2]))
             except (ValueError, IndexError):
                 continue
+            try:
+                power.append(float(r[3]))
+            except (ValueError, IndexError):
+                pass
             for n, v in zip(names, r[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if power:
+            out["power_w_median"] = statistics.median(power)
+        return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle (reference arm)
 
-def oracle_step(inp, rows: np.ndarray, chunks: int):
-    """The hot path on the CPU oracle for a sample of query rows (all heads, all keys): prologue, chunked attention, merge."""
-    import oracle
+class OracleInputs:
+    """The workload's inputs as fp64 arrays for the oracle (converted once; the key side is reused by every
+    sampled row)."""
 
-    orc = oracle.get()
-    w = inp.w
-    c64, s64 = inp.cos.astype(np.float64), inp.sin.astype(np.float64)
-    q = inputs.bf16_bits_to_f64(inp.q[:, rows])
-    k = inputs.bf16_bits_to_f64(inp.k)
-    v = inputs.bf16_bits_to_f64(inp.v)
-    if w.prologue:
-        q = oracle.round_bf16(orc.qk_norm_rope(q, inp.wq.astype(np.float64), c64[rows], s64[rows], w.eps))
-        k = oracle.round_bf16(orc.qk_norm_rope(k, inp.wk.astype(np.float64), c64, s64, w.eps))
-    parts = [orc.attention(q, k, v, w.scale, lo, hi) for lo, hi in w.chunk_bounds(chunks)]
-    return orc.merge_lse(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    def __init__(self, inp, chunks: int):
+        import oracle
+
+        self.orc = oracle.get()
+        self.inp = inp
+        self.chunks = chunks
+        w = inp.w
+        self.c64, self.s64 = inp.cos.astype(np.float64), inp.sin.astype(np.float64)
+        k = inputs.bf16_bits_to_f64(inp.k)
+        if w.prologue:
+            k = oracle.round_bf16(self.orc.qk_norm_rope(k, inp.wk.astype(np.float64), self.c64, self.s64, w.eps))
+        self.k = k
+        self.v = inputs.bf16_bits_to_f64(inp.v)
+
+    def step(self, rows: np.ndarray):
+        """The hot path on the oracle for a sample of query rows (all heads, all keys): prologue of those rows,
+        attention over every KV chunk, merge."""
+        import oracle
+
+        w = self.inp.w
+        q = inputs.bf16_bits_to_f64(self.inp.q[:, rows])
+        if w.prologue:
+            q = oracle.round_bf16(self.orc.qk_norm_rope(q, self.inp.wq.astype(np.float64), self.c64[rows],
+                                                        self.s64[rows], w.eps))
+        parts = [self.orc.attention(q, self.k, self.v, w.scale, lo, hi) for lo, hi in w.chunk_bounds(self.chunks)]
+        return self.orc.merge_lse(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
 
 
 def cpu_sample_rows(w, n: int) -> np.ndarray:
@@ -154,21 +196,23 @@ def cpu_baseline(inp, chunks: int, budget_s: float = 15.0):
     import oracle
 
     w = inp.w
-    n, total_t, total_f = 16, 0.0, 0.0
+    ref = OracleInputs(inp, chunks)
+    n, total_t, total_f = 8, 0.0, 0.0
     while True:
         rows = cpu_sample_rows(w, min(n, w.S))
         t0 = time.perf_counter()
-        oracle_step(inp, rows, chunks)
+        ref.step(rows)
         dt = time.perf_counter() - t0
         total_t += dt
         total_f += 4.0 * w.B * w.H * len(rows) * w.S * w.D
         if total_t >= budget_s or n >= w.S:
             break
-        n = min(w.S, max(2 * n, int(n * budget_s / max(dt, 1e-3) / 2)))
+        n = min(w.S, max(2 * n, int(n * (budget_s - total_t) / max(dt, 1e-3))))
     return {"value": total_f / total_t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{w.name}: prologue on all keys + attention over {chunks} KV chunks + merge for evenly spaced "
-                      f"query rows (all {w.H} heads, all {w.S} keys), row counts doubling to {len(rows)}; "
-                      f"{total_t:.1f} s of fp64 C/OpenMP work in total"}
+            "sample": f"{w.name}: attention over {chunks} KV chunks + merge (and the prologue, where the workload "
+                      f"has one) for evenly spaced query rows, all {w.H} heads, all {w.S} keys; row counts growing "
+                      f"to {len(rows)}; {total_t:.1f} s of fp64 C/OpenMP work in total (the key-side fp64 "
+                      f"conversion, done once, is not timed)"}
 
 
 def run_reference(args):
@@ -180,17 +224,18 @@ def run_reference(args):
     inp = inputs.make_inputs(args.workload)
     w = inp.w
     chunks = args.chunks or w.chunks
+    ref = OracleInputs(inp, chunks)
     rows = cpu_sample_rows(w, args.ref_rows)
     for _ in range(args.warmup):
-        oracle_step(inp, rows, chunks)
+        ref.step(rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(inp, rows, chunks)
+        ref.step(rows)
     dt = time.perf_counter() - t0
     flops = 4.0 * w.B * w.H * len(rows) * w.S * w.D * args.steps
     value = flops / dt / 1e12
-    sample = (f"{w.name}: {len(rows)} evenly spaced query rows per (b, h) against all {w.S} keys; prologue, "
-              f"{chunks} KV chunks and merge on the fp64 oracle")
+    sample = (f"{w.name}: {len(rows)} evenly spaced query rows per (b, h) against all {w.S} keys; "
+              f"{chunks} KV chunks and merge (and the prologue, where the workload has one) on the fp64 oracle")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
@@ -206,14 +251,17 @@ def merge_mode(w, args):
     return args.merge if args.merge != "auto" else MERGE[w.name]
 
 
+def merge_text(merge: str, chunks: int) -> str:
+    if chunks <= 1:
+        return "none (one KV chunk)"
+    return "update (fused in each later chunk's epilogue)" if merge == "update" else "kernel (LSE-merge kernel)"
+
+
 def config_of(w, chunks, args):
     return {"workload": w.description, "name": w.name, "B": w.B, "H": w.H, "D": w.D, "Sq": w.S, "Skv": w.S,
-            "kv_chunks": chunks, "partial_o": PARTIAL[w.name],
-            "merge": (merge_mode(w, args) + (" (fused in the last chunk's epilogue)" if merge_mode(w, args) == "update"
-                                             else " (LSE-merge kernel)")) if chunks > 1 else "none",
+            "kv_chunks": chunks, "partial_o": PARTIAL[w.name], "merge": merge_text(merge_mode(w, args), chunks),
             "prologue": w.prologue, "causal": False,
             "launch_overlap": not getattr(args, "no_launch_overlap", False),
-            "attention_variant": getattr(args, "attention_variant", 0),
             "scale": "1/sqrt(D)", "l2": "flushed before every timed step (512 MiB write)",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
@@ -225,9 +273,10 @@ def attn_traffic(name: str):
     import hashlib
 
     src = ROOT / "diffusion_transformer_attention_dit_gb300" / "csrc" / "attn_fwd.cu"
-    if hashlib.sha256(src.read_bytes()).hexdigest()[:16] != ATTN_TRAFFIC["source_sha256_prefix"]:
+    if ATTN_TRAFFIC["source_sha256_prefix"] is None or \
+            hashlib.sha256(src.read_bytes()).hexdigest()[:16] != ATTN_TRAFFIC["source_sha256_prefix"]:
         return None
-    return ATTN_TRAFFIC.get(name)
+    return ATTN_TRAFFIC["by_workload"].get(name)
 
 
 def aggregate(t_local: float, flops_per_step: float, steps: int, world: int, device=None):
@@ -246,6 +295,242 @@ def aggregate(t_local: float, flops_per_step: float, steps: int, world: int, dev
     return t_max, flops_per_step * steps * world / t_max / 1e12
 
 
+def merge_bytes(C, B, S, H, D, s_in, s_out):
+    """Algorithmic bytes of one merge: C partial O and LSE slabs in, one O and LSE out."""
+    return C * B * S * H * D * s_in + 4 * C * B * H * S + B * S * H * D * s_out + 4 * B * H * S
+
+
+def prologue_bytes(B, S, H, D):
+    """Algorithmic bytes of one prologue: q, k read and q', k' written (bf16), cos/sin tables, two weights."""
+    return 8 * B * S * H * D + 4 * S * D + 8 * D
+
+
+class Device:
+    """Device-side state of one workload: inputs, outputs, workspace, the L2 flush buffer."""
+
+    def __init__(self, inp, chunks, merge, dev):
+        import torch
+
+        from diffusion_transformer_attention_dit_gb300 import ops
+
+        w = inp.w
+        self.w, self.inp, self.chunks, self.merge, self.dev = w, inp, chunks, merge, dev
+        self.pdt = torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+        self.q, self.k, self.v = bf(inp.q), bf(inp.k), bf(inp.v)
+        self.tabs = [torch.from_numpy(a).to(dev) for a in (inp.wq, inp.wk, inp.cos, inp.sin)]
+        B, S, H, D = w.B, w.S, w.H, w.D
+        self.o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(max(1, ops.attention_workspace_bytes(B, S, H, D, chunks, w.prologue, self.pdt, merge)),
+                              dtype=torch.uint8, device=dev)
+        self.merge_kernel = chunks > 1 and merge == "kernel"
+        self.launches = (1 if w.prologue else 0) + chunks + (1 if self.merge_kernel else 0)
+
+    def step(self, attn_events=None):
+        from diffusion_transformer_attention_dit_gb300 import ops
+
+        ops.dit_attention(self.q, self.k, self.v, *self.tabs, eps=self.w.eps, chunks=self.chunks,
+                          partial_dtype=self.pdt, prologue=self.w.prologue, merge=self.merge, o=self.o, lse=self.lse,
+                          workspace=self.ws, attn_events=attn_events)
+
+
+def made_events(n, stream):
+    """Events created and recorded once before a timed region, so none is created inside it."""
+    import torch
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record(stream)
+    return evs
+
+
+def steps_for(dev_state, seconds: float, cap: int = 4000) -> int:
+    """Steps that fill about `seconds` of timed work (one flushed step is measured first)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dev_state.flush.zero_()
+    e0.record(stream)
+    dev_state.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return int(min(cap, max(10, seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3))))
+
+
+def time_workload(ds, steps, uuid, world=1):
+    """The step region (events around whole steps only), then the attention region (events right before the first
+    and after the last attention launch of each step, and after the merge kernel when there is one).  Returns the
+    summed seconds and each region's clock record."""
+    import torch
+    import torch.distributed as dist
+
+    from diffusion_transformer_attention_dit_gb300 import ops
+
+    stream = torch.cuda.current_stream()
+    res = {}
+    # Timed region: whole steps only.  Events between the kernels of a step stall the stream and cut the launch
+    # overlap between them, so the step region carries none.
+    step_ev = made_events(2 * steps, stream)
+    with ClockSampler(uuid) as clocks:
+        clocks.ready()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            ds.flush.zero_()
+            step_ev[2 * i].record(stream)
+            ds.step()
+            step_ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+        if world > 1:
+            dist.barrier()
+    ops.poll_device_error()
+    res["t_steps"] = sum(step_ev[2 * i].elapsed_time(step_ev[2 * i + 1]) for i in range(steps)) / 1e3
+    res["clocks_steps"] = clocks.summary(wall0, wall1)
+    res["wall_steps"] = wall1 - wall0
+    # Attention region: dit_attention records its events on this stream right before the first and after the last
+    # attention launch; one more event after the call closes the merge kernel.
+    attn_steps = min(steps, 1000)
+    n_ev = 3 if ds.merge_kernel else 2
+    ev = made_events(n_ev * attn_steps, stream)
+    with ClockSampler(uuid) as clocks:
+        clocks.ready()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(attn_steps):
+            ds.flush.zero_()
+            e = ev[n_ev * i:n_ev * (i + 1)]
+            ds.step((e[0], e[1]))
+            if ds.merge_kernel:
+                e[2].record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+    ops.poll_device_error()
+    res["attn_steps"] = attn_steps
+    res["t_attn"] = sum(ev[n_ev * i].elapsed_time(ev[n_ev * i + 1]) for i in range(attn_steps)) / 1e3
+    if ds.merge_kernel:
+        res["t_merge"] = sum(ev[n_ev * i + 1].elapsed_time(ev[n_ev * i + 2]) for i in range(attn_steps)) / 1e3
+    res["clocks_attn"] = clocks.summary(wall0, wall1)
+    return res
+
+
+def time_prologue_alone(ds, uuid, seconds: float = REGION_S):
+    """The prologue kernel alone at the workload's shapes (L2 flushed before every launch), for about `seconds`."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import ops
+
+    stream = torch.cuda.current_stream()
+    qo, ko = torch.empty_like(ds.q), torch.empty_like(ds.k)
+    run = lambda: ops.qk_norm_rope(ds.q, ds.k, *ds.tabs, ds.w.eps, q_out=qo, k_out=ko)  # noqa: E731
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = int(min(20000, max(20, seconds * 1e3 / (e0.elapsed_time(e1) + 0.1))))
+    ev = made_events(2 * n, stream)
+    with ClockSampler(uuid) as clocks:
+        clocks.ready()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(n):
+            ds.flush.zero_()
+            ev[2 * i].record(stream)
+            run()
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+    ops.poll_device_error()
+    ts = [ev[2 * i].elapsed_time(ev[2 * i + 1]) / 1e3 for i in range(n)]
+    del qo, ko
+    return statistics.median(ts), n, clocks.summary(wall0, wall1)
+
+
+def hbm_record(name, t_s, nbytes, peak_gbs, launches, clocks, how):
+    gbs = nbytes / t_s / 1e9
+    return {"kernel": name, "bytes": nbytes, "us": t_s * 1e6, "GB/s": gbs, "peak": peak_gbs, "frac": gbs / peak_gbs,
+            "launches": launches, "timing": how, "clocks": clocks}
+
+
+def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
+    """The public host-buffer entry point (dit_attention_host) on pinned host inputs, copies inside the timed
+    region; returns (seconds summed over the steps, h2d bytes, d2h bytes)."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import ops
+
+    w = inp.w
+    B, S, H, D = w.B, w.S, w.H, w.D
+    pdt = torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16
+    pin = {n: torch.from_numpy(np.ascontiguousarray(getattr(inp, n)).view(np.int16)).pin_memory()
+           for n in ("q", "k", "v")}
+    hq, hk, hv = (pin[n].view(torch.bfloat16).view(B, S, H, D) for n in ("q", "k", "v"))
+    small = [torch.from_numpy(a).pin_memory() for a in (inp.wq, inp.wk, inp.cos, inp.sin)] if w.prologue else []
+    o_host = torch.empty((B, S, H, D), dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(pin.values()) + small)
+    d2h = o_host.numel() * 2 + lse_host.numel() * 4
+    ws = torch.empty(ops.attention_host_workspace_bytes(B, S, H, D, chunks, w.prologue, pdt, merge=merge),
+                     dtype=torch.uint8, device=dev)
+    tabs = small if w.prologue else [None] * 4
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        ops.dit_attention_host(hq, hk, hv, *tabs, eps=w.eps, chunks=chunks, partial_dtype=pdt, prologue=w.prologue,
+                               merge=merge, o=o_host, lse=lse_host, workspace=ws)
+
+    for _ in range(max(1, warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    t = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t += e0.elapsed_time(e1) / 1e3
+    ops.poll_device_error()
+    del ws
+    return t, h2d, d2h
+
+
+def per_workload_record(name, args, dev, uuid, pk, src):
+    """One of the other full-size workloads: its step and attention regions, with their clocks."""
+    import torch
+
+    inp = inputs.make_inputs(name)
+    w = inp.w
+    chunks = w.chunks
+    merge = MERGE[name]
+    ds = Device(inp, chunks, merge, dev)
+    for _ in range(args.warmup):
+        ds.step()
+    steps = steps_for(ds, REGION_S)
+    r = time_workload(ds, steps, uuid)
+    flops = w.attention_flops()
+    attn = flops * r["attn_steps"] / r["t_attn"] / 1e12
+    rec = {"workload": w.description, "B": w.B, "H": w.H, "D": w.D, "S": w.S, "kv_chunks": chunks,
+           "merge": merge_text(merge, chunks), "partial_o": PARTIAL[name], "prologue": w.prologue,
+           "steps": steps, "ms_per_step": r["t_steps"] / steps * 1e3,
+           "step_tflops": flops * steps / r["t_steps"] / 1e12,
+           "attention_tflops": attn, "attention_frac": attn / pk["bf16_tflops"],
+           "attention_frac_sustained": attn / pk["bf16_tflops_sustained"], "peak_source": src,
+           "clocks": r["clocks_steps"], "clocks_attention": r["clocks_attn"]}
+    del ds
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -261,163 +546,91 @@ def run_ours(args):
     build.build()
     ops.load_library()
     ops.set_launch_overlap(not args.no_launch_overlap)
-    ops.set_attention_variant(args.attention_variant)
-
-    inp = inputs.make_inputs(args.workload)
-    w = inp.w
-    chunks = args.chunks or w.chunks
-    pdt = torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16
     dev = torch.device("cuda", torch.cuda.current_device())
-
-    def to_dev(a, dtype=None):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return t.to(dev).view(torch.bfloat16) if dtype is None else t.to(dev)
-
-    host = {"q": inp.q, "k": inp.k, "v": inp.v}
-    q, k, v = (to_dev(host[n].view(np.int16)) for n in ("q", "k", "v"))
-    wq, wk, cos, sin = (torch.from_numpy(a).to(dev) for a in (inp.wq, inp.wk, inp.cos, inp.sin))
-    B, S, H, D = w.B, w.S, w.H, w.D
-    o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    merge = merge_mode(w, args)
-    launches_per_step = (1 if w.prologue else 0) + chunks + (1 if chunks > 1 and merge == "kernel" else 0)
-    # one C call per step (dit_attention): prologue into the workspace, the KV chunks (chunk c covers keys
-    # [c*S/chunks, (c+1)*S/chunks)), then the merge -- in the update form in the last chunk's epilogue, else by
-    # the merge kernel over stacked partials.  The events bracket the attention launches alone.
-    ws = torch.empty(max(1, ops.attention_workspace_bytes(B, S, H, D, chunks, w.prologue, pdt, merge)),
-                     dtype=torch.uint8, device=dev)
-
-    def step(attn_events=None):
-        ops.dit_attention(q, k, v, wq, wk, cos, sin, eps=w.eps, chunks=chunks, partial_dtype=pdt,
-                          prologue=w.prologue, merge=merge, o=o, lse=lse, workspace=ws, attn_events=attn_events)
-
-    for _ in range(args.warmup):
-        step()
-    ops.poll_device_error()
-    if not args.steps:
-        # enough steps for about 2 s of timed work (so the clock sampler sees the region)
-        e0, e1 = ev(), ev()
-        flush.zero_()
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        args.steps = int(min(4000, max(10, 2000.0 / max(e0.elapsed_time(e1), 1e-3))))
-
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:  # noqa: BLE001
         pass
-    def made(n):  # events created (recorded once) before a timed region, so none is created inside it
-        evs = [ev() for _ in range(n)]
-        for e in evs:
-            e.record(stream)
-        return evs
+    pk, src = peaks()
 
-    # Timed region: whole steps only.  Events between the kernels of a step stall the stream and cut the launch
-    # overlap between them (about 11 us per Qwen-Image step), so the step region carries none; the attention
-    # launches are timed in a second region of the same steps below.
-    step_ev = made(2 * args.steps)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    with ClockSampler(uuid) as clocks:
-        for i in range(args.steps):
-            flush.zero_()
-            step_ev[2 * i].record(stream)
-            step()
-            step_ev[2 * i + 1].record(stream)
-        torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    if world > 1:
-        dist.barrier()
+    inp = inputs.make_inputs(args.workload)
+    w = inp.w
+    chunks = args.chunks or w.chunks
+    merge = merge_mode(w, args)
+    ds = Device(inp, chunks, merge, dev)
+    for _ in range(args.warmup):
+        ds.step()
     ops.poll_device_error()
-    t_steps = sum(step_ev[2 * i].elapsed_time(step_ev[2 * i + 1]) for i in range(args.steps)) / 1e3
-    # Attention region: the same steps with events recorded (by dit_attention, on this stream) right before the
-    # first and after the last attention launch; achieved = attention flops / the time between them.
-    attn_steps = min(args.steps, ATTN_TIMED_STEPS)
-    attn_ev = made(2 * attn_steps)
-    torch.cuda.synchronize()
-    for i in range(attn_steps):
-        flush.zero_()
-        step((attn_ev[2 * i], attn_ev[2 * i + 1]))
-    torch.cuda.synchronize()
-    ops.poll_device_error()
-    t_attn = sum(attn_ev[2 * i].elapsed_time(attn_ev[2 * i + 1]) for i in range(attn_steps)) / 1e3
+    if not args.steps:
+        args.steps = steps_for(ds, 2.0)
+    r = time_workload(ds, args.steps, uuid, world)
     flops_step = w.attention_flops()
-    t_max, value = aggregate(t_steps, flops_step, args.steps, world, dev)
+    t_max, value = aggregate(r["t_steps"], flops_step, args.steps, world, dev)
+    B, S, H, D = w.B, w.S, w.H, w.D
 
-    # end to end through the public API: pinned host inputs in, O and LSE back to pinned host memory
-    pin = {n: torch.from_numpy(np.ascontiguousarray(host[n]).view(np.int16)).pin_memory() for n in host}
-    pin_small = [torch.from_numpy(a).pin_memory() for a in (inp.wq, inp.wk, inp.cos, inp.sin)]
-    o_host = torch.empty((B, S, H, D), dtype=torch.bfloat16).pin_memory()
-    lse_host = torch.empty((B, H, S), dtype=torch.float32).pin_memory()
-    h2d = sum(t_.numel() * t_.element_size() for t_ in list(pin.values()) + pin_small)
-    d2h = o_host.numel() * 2 + lse_host.numel() * 4
-    dq, dk, dv = (torch.empty((B, S, H, D), dtype=torch.int16, device=dev) for _ in range(3))
-    dsmall = [torch.empty_like(t_, device=dev) for t_ in pin_small]
+    hbm = {}
+    if r.get("t_merge") is not None:
+        s_in = 4 if PARTIAL[w.name] == "f32" else 2
+        hbm["merge_lse"] = hbm_record(
+            "merge_lse_bulk_kernel", r["t_merge"] / r["attn_steps"], merge_bytes(chunks, B, S, H, D, s_in, 2),
+            pk["hbm_gbs"], r["attn_steps"], r["clocks_attn"],
+            f"the step's merge kernel ({chunks} {PARTIAL[w.name]} partials -> bf16), events around it in the "
+            "attention region of the same steps, mean per launch")
+    if not args.no_hbm:
+        t_pro, n_pro, clk_pro = time_prologue_alone(ds, uuid)
+        hbm["qk_norm_rope"] = hbm_record(
+            "qk_norm_rope_kernel", t_pro, prologue_bytes(B, S, H, D), pk["hbm_gbs"], n_pro, clk_pro,
+            f"the prologue kernel alone on this workload's q, k, weights and rotary tables (the step "
+            f"{'runs it' if w.prologue else 'has none'}), L2 flushed before every launch, median")
 
-    host_path = merge == "update" or chunks == 1
-    if host_path:
-        # dit_attention_host: the C entry point that copies the inputs in (value rows chunk by chunk on a copy
-        # stream, overlapping the kernels), runs the path and copies O and LSE out
-        hq, hk, hv = (pin[n].view(torch.bfloat16).view(B, S, H, D) for n in ("q", "k", "v"))
-        ws = torch.empty(ops.attention_host_workspace_bytes(B, S, H, D, chunks, w.prologue, pdt), dtype=torch.uint8,
-                         device=dev)
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        t_e2e, h2d, d2h = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
+        _, e2e_value = aggregate(t_e2e, flops_step, e2e_steps, world, dev)
+        e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "ms_per_step": t_e2e / e2e_steps * 1e3,
+               "api": "dit_attention_host (" + ("query ranges, stacked partials + merge kernel per range, each "
+                                                "range's O copied back while the next computes" if
+                                                (merge == "kernel" or chunks == 1) else
+                                                "value rows pipelined per KV chunk, update-form merge") + ")"}
+    launches = ds.launches * args.steps
+    del ds
+    torch.cuda.empty_cache()
 
-    def e2e_step():
-        if host_path:
-            ops.dit_attention_host(hq, hk, hv, *pin_small, eps=w.eps, chunks=chunks, partial_dtype=pdt,
-                                   prologue=w.prologue, o=o_host, lse=lse_host, workspace=ws)
-            return
-        for src, dst in zip((pin["q"], pin["k"], pin["v"]), (dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
-        for src, dst in zip(pin_small, dsmall):
-            dst.copy_(src, non_blocking=True)
-        oo, ll = ops.dit_attention(dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16),
-                                   *dsmall, eps=w.eps, chunks=chunks, partial_dtype=pdt, prologue=w.prologue,
-                                   merge=merge)
-        o_host.copy_(oo, non_blocking=True)
-        lse_host.copy_(ll, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_t = 0.0
-    for _ in range(args.steps):
-        flush.zero_()
-        e0, e1 = ev(), ev()
-        e0.record(stream)
-        e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_t += e0.elapsed_time(e1) / 1e3
-    _, e2e_value = aggregate(e2e_t, flops_step, args.steps, world, dev)
+    per = {}
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        for name in PER_WORKLOAD:
+            if name != w.name:
+                per[name] = per_workload_record(name, args, dev, uuid, pk, src)
 
     if rank == 0:
-        peak_tf, peak_gbs, src = peaks()
-        achieved = flops_step * attn_steps / t_attn / 1e12
+        achieved = flops_step * r["attn_steps"] / r["t_attn"] / 1e12
+        traffic = args.traffic if args.traffic is not None else attn_traffic(w.name)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(w, chunks, args),
-            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved, "peak": peak_tf,
-                         "unit": "TFLOP/s", "frac": achieved / peak_tf, "peak_source": src,
-                         "traffic": args.traffic if args.traffic is not None else attn_traffic(w.name),
-                         "timing": f"{attn_steps} further steps with events right before the first and after the "
-                                   "last attention launch (the step region carries no events between kernels)"},
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "api": "dit_attention_host (copies pipelined per KV chunk)" if host_path
-                    else "torch copies + ops.dit_attention"},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(),
-            "wall_s_timed_region": wall,
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": achieved,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "peak_kind": "burst (cuBLAS bf16 GEMM, best of 10)",
+                         "peak_sustained": pk["bf16_tflops_sustained"],
+                         "frac_sustained": achieved / pk["bf16_tflops_sustained"], "peak_source": src,
+                         "traffic": traffic,
+                         "traffic_source": (ATTN_TRAFFIC["capture"] if traffic is not None and args.traffic is None
+                                            else "given on the command line" if traffic is not None else
+                                            "none for this attention source"),
+                         "timing": f"{r['attn_steps']} further steps with events right before the first and after "
+                                   "the last attention launch (the step region carries no events between kernels)",
+                         "clocks": r["clocks_attn"]},
+            "hbm": hbm,
+            "per_workload": per,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": r["clocks_steps"],
+            "wall_s_timed_region": r["wall_steps"],
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(inp, chunks, args.cpu_budget)
@@ -478,9 +691,9 @@ def run_ring_overlap(args):
 
 def run_hbm_kernels(args):
     """Diagnostic: each HBM-bound kernel alone at the workload's shapes (synthetic inputs, L2 flushed before every
-    timed launch, CUDA events, median of the steps): prologue, LSE merge of the workload's chunk count (8 for a
-    one-chunk workload), LayerNorm-modulate and RMSNorm over C = H*D, fp8 quantiser.  Achieved = algorithmic bytes /
-    time."""
+    timed launch, CUDA events, median over about REGION_S seconds of launches, each kernel with its own clock
+    record): prologue, LSE merge of the workload's chunk count (8 for a one-chunk workload), LayerNorm-modulate
+    and RMSNorm over C = H*D, fp8 quantiser.  Achieved = algorithmic bytes / time."""
     import torch
 
     from diffusion_transformer_attention_dit_gb300 import build, ops
@@ -493,45 +706,64 @@ def run_hbm_kernels(args):
     C = w.chunks if w.chunks > 1 else 8
     pdt = torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16
     dev = torch.device("cuda")
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001
+        pass
     g = torch.Generator(device=dev)
     g.manual_seed(1234 + w.index)
     rnd = lambda *shape: torch.randn(*shape, device=dev, generator=g)  # noqa: E731
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
 
     def timed(fn):
         for _ in range(max(args.warmup, 3)):
             fn()
-        ts = []
-        for _ in range(max(args.steps, 5)):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        n = int(min(20000, max(max(args.steps, 5), REGION_S * 1e3 / (e0.elapsed_time(e1) + 0.1))))
+        ev = made_events(2 * n, stream)
+        with ClockSampler(uuid) as clocks:
+            clocks.ready()
             torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e3)
+            wall0 = time.perf_counter()
+            for i in range(n):
+                flush.zero_()
+                ev[2 * i].record(stream)
+                fn()
+                ev[2 * i + 1].record(stream)
+            torch.cuda.synchronize()
+            wall1 = time.perf_counter()
         ops.poll_device_error()
-        return statistics.median(ts)
+        return statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(n)), n, \
+            clocks.summary(wall0, wall1)
 
-    peak_tf, peak_gbs, src = peaks()
+    pk, src = peaks()
     res = {}
 
-    def record(name, us, nbytes):
+    def record(name, timing, nbytes):
+        us, n, clk = timing
         gbs = nbytes / us / 1e3
-        res[name] = {"us": us, "GB": nbytes / 1e9, "GB/s": gbs, "frac": gbs / peak_gbs}
+        res[name] = {"us": us, "GB": nbytes / 1e9, "GB/s": gbs, "frac": gbs / pk["hbm_gbs"], "launches": n,
+                     "clocks": clk}
 
     q, k = rnd(B, S, H, D).to(torch.bfloat16), rnd(B, S, H, D).to(torch.bfloat16)
     wq, wk = 1 + 0.1 * rnd(D), 1 + 0.1 * rnd(D)
     cos, sin = rnd(S, D // 2), rnd(S, D // 2)
     qo, ko = torch.empty_like(q), torch.empty_like(k)
     record("qk_norm_rope", timed(lambda: ops.qk_norm_rope(q, k, wq, wk, cos, sin, w.eps, q_out=qo, k_out=ko)),
-           8 * B * S * H * D + 4 * S * D + 8 * D)
+           prologue_bytes(B, S, H, D))
     del k, ko
     parts = rnd(C, B, S, H, D).to(pdt)
     lse_parts = 3 + 2 * rnd(C, B, H, S)
     lse = torch.empty(B, H, S, device=dev)
-    record(f"merge_lse C={C} {PARTIAL[w.name]}->bf16", timed(lambda: ops.attn_merge_lse(parts, lse_parts, o=qo, lse=lse)),
-           C * B * S * H * D * parts.element_size() + 4 * C * B * H * S + 2 * B * S * H * D + 4 * B * H * S)
+    record(f"merge_lse C={C} {PARTIAL[w.name]}->bf16",
+           timed(lambda: ops.attn_merge_lse(parts, lse_parts, o=qo, lse=lse)),
+           merge_bytes(C, B, S, H, D, parts.element_size(), 2))
     del parts, lse_parts
     x, y = q.view(B, S, H * D), qo.view(B, S, H * D)
     Cc = H * D
@@ -543,7 +775,7 @@ def run_hbm_kernels(args):
     scales = torch.empty(B * S, dtype=torch.float32, device=dev)
     record("quant_fp8_rows", timed(lambda: ops.quant_fp8_rows(x.view(B * S, Cc), codes, scales)),
            3 * B * S * Cc + 4 * B * S)
-    print(json.dumps({"mode": "hbm_kernels", "workload": w.name, "peak_GBps": peak_gbs, "peak_source": src,
+    print(json.dumps({"mode": "hbm_kernels", "workload": w.name, "peak_GBps": pk["hbm_gbs"], "peak_source": src,
                       "kernels": res}))
 
 
@@ -592,19 +824,18 @@ def main():
     ap.add_argument("--steps", type=int, default=0, help="timed steps (0: about 2 s worth)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen_image", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="wan720", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--chunks", type=int, default=0, help="KV chunks (0: the workload's own)")
-    ap.add_argument("--attention-variant", type=int, choices=[0, 1, 2, 3, 4], default=0,
-                    help="attention kernel for head dim 128: 0 default, 1 one CTA (P in TMEM), 2 CTA pairs with two "
-                         "tiles per CTA, 3 CTA pairs with one tile per CTA and three S buffers, 4 one CTA with P in "
-                         "shared memory")
     ap.add_argument("--no-launch-overlap", action="store_true",
                     help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
     ap.add_argument("--merge", choices=["auto", "kernel", "update"], default="auto",
                     help="combine KV chunks by the merge kernel or in the attention epilogue (auto: the workload's)")
-    ap.add_argument("--ref-rows", type=int, default=48, help="query rows per (b, h) in each reference step")
+    ap.add_argument("--ref-rows", type=int, default=16, help="query rows per (b, h) in each reference step")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip the per_workload record")
+    ap.add_argument("--no-hbm", action="store_true", help="skip the prologue-alone entry of the hbm record")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--ring-overlap", type=int, default=0, metavar="RANKS",
                     help="time the one-GPU ring-overlap emulation with RANKS key shards instead (diagnostic)")
     ap.add_argument("--hbm-kernels", action="store_true",

@@ -14,7 +14,6 @@ namespace {
 
 thread_local const char *g_detail = "";
 std::atomic<int> g_launch_overlap{1};
-std::atomic<int> g_attention_variant{0};
 
 dit_status fail(dit_status s, const char *why) {
   g_detail = why;
@@ -44,16 +43,8 @@ dit_status from_cuda(cudaError_t e, const char *detail) {
 
 bool ditattn::launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
 void ditattn::set_error_detail(const char *why) { g_detail = why; }
-int ditattn::attention_variant() { return g_attention_variant.load(std::memory_order_relaxed); }
 
 extern "C" {
-
-dit_status dit_set_attention_variant(int variant) {
-  g_detail = "";
-  if (variant < 0 || variant > 4) return fail(DIT_ERR_INVALID_ARG, "variant must be 0 to 4");
-  g_attention_variant.store(variant, std::memory_order_relaxed);
-  return DIT_OK;
-}
 
 dit_status dit_set_launch_overlap(int enable) {
   g_detail = "";
@@ -175,10 +166,13 @@ dit_status ditattn::attn_checked(const void *q, const void *k, const void *v, in
                                  const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin,
                                  int kv_end, bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3],
                                  float *lse, const void *o_acc, dit_dtype acc_dtype, const int64_t acc_strides[3],
-                                 const float *lse_acc, bool defer_wait, cudaStream_t stream) {
+                                 const float *lse_acc, int sequence_chunk, cudaStream_t stream) {
+  // Only a later chunk of a chunk sequence may defer its dependency wait: its
+  // predecessor on the stream is the previous chunk, which itself waited at its
+  // start (chunk 0) or deferred under this same rule.
   return attn_common(q, k, v, B, H, Sq, Skv, D, q_strides, kv_strides, scale, kv_begin, kv_end, causal, o, o_dtype,
                      o_strides, lse, reinterpret_cast<struct CUstream_st *>(stream), o_acc != nullptr, o_acc,
-                     acc_dtype, acc_strides, lse_acc, defer_wait);
+                     acc_dtype, acc_strides, lse_acc, sequence_chunk >= 1);
 }
 
 extern "C" {
@@ -248,12 +242,10 @@ dit_status dit_poll_device_error(struct CUstream_st *stream) {
   if (e == cudaSuccess) e = ditattn::read_and_clear_attn_error(&va);
   if (e == cudaSuccess) e = ditattn::read_and_clear_prologue_error(&vp);
   if (e == cudaSuccess) e = ditattn::read_and_clear_merge_error(&vm);
-  unsigned int vf = 0, vq = 0, vs = 0;
+  unsigned int vf = 0;
   if (e == cudaSuccess) e = ditattn::read_and_clear_fp8_error(&vf);
-  if (e == cudaSuccess) e = ditattn::read_and_clear_pair_error(&vq);
-  if (e == cudaSuccess) e = ditattn::read_and_clear_ps_error(&vs);
   if (e != cudaSuccess) return from_cuda(e, nullptr);
-  if (va | vp | vm | vf | vq | vs) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
+  if (va | vp | vm | vf) return fail(DIT_ERR_TIMEOUT, "a bounded device-side wait gave up");
   return DIT_OK;
 }
 

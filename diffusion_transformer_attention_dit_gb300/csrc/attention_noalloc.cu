@@ -9,14 +9,18 @@
 // taken from a fixed scratch array that is part of the library itself.
 //
 //   - The scratch is one file-scope static device array of kScratchBytes
-//     (32 MiB).  The CUDA runtime places it on a device when the first call on
-//     that device uses it (device data of a library is loaded on first use),
-//     and it stays reserved until the process exits.  Requests whose
-//     workspace would not fit are refused (DIT_ERR_UNSUPPORTED) before
-//     anything is launched.
-//   - The array's device address is looked up once per device
-//     (cudaGetSymbolAddress, with that device current) by the first call made
-//     on that device; make that first call before any stream capture.
+//     (32 MiB).  With the CUDA runtime's default lazy module loading, the array
+//     is placed on a device when the first call on that device uses it and it
+//     stays reserved until the process exits; with eager loading
+//     (CUDA_MODULE_LOADING=EAGER) every device on which the process creates a
+//     context reserves it as soon as the library's module is loaded, whether or
+//     not this entry point is ever called.  Requests whose workspace would not
+//     fit are refused (DIT_ERR_UNSUPPORTED) before anything is launched.
+//   - Every call looks the array's device address up again
+//     (cudaGetSymbolAddress, with the call's device current), so a context
+//     that was torn down and rebuilt (cudaDeviceReset) is never handed a stale
+//     address.  The first call on a device may load the library's module
+//     there; make that first call before any stream capture.
 //   - All calls share the array.  Nothing in it has to start at zero (every
 //     byte a call reads, that call has written first), but calls that run at
 //     the same time on the GPU -- on different streams, or different host
@@ -24,8 +28,6 @@
 //   - No cudaMalloc, cudaFree or allocating library routine is called.
 
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "../../include/ditattn.h"
 #include "internal.h"
@@ -40,24 +42,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 namespace {
 
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[64] = {};
-
 // Device address of the scratch array on the current device (host code may not
-// use the array's name as an address).
+// use the array's name as an address).  Looked up on every call: the lookup is
+// cheap once the module is loaded, and a cached address would outlive a reset
+// of the device's context.
 cudaError_t scratch_address(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

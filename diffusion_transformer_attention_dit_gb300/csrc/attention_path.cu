@@ -67,22 +67,22 @@ dit_status ditattn::run_attention_chunks(const void *q, const void *k, const voi
   for (int c = 0; c < chunks; ++c) {
     const int lo = (int)((int64_t)c * S / chunks), hi = (int)((int64_t)(c + 1) * S / chunks);
     if (before_chunk && (e = before_chunk(ctx, c)) != cudaSuccess) return fail(DIT_ERR_CUDA, cudaGetErrorString(e));
-    const bool defer = c > 0, last = c == chunks - 1;
+    const bool last = c == chunks - 1;
     dit_status r;
     if (chunks == 1) {
       r = attn_checked(q, k, v, B, H, S, S, D, st, st, scale, lo, hi, false, o, o_dtype, st, lse, nullptr, DIT_BF16,
-                       nullptr, nullptr, false, stream);
+                       nullptr, nullptr, -1, stream);
     } else if (merge_update) {
       if (c == 0)
         r = attn_checked(q, k, v, B, H, S, S, D, st, st, scale, lo, hi, false, acc, partial_dtype, st, lse, nullptr,
-                         DIT_BF16, nullptr, nullptr, false, stream);
+                         DIT_BF16, nullptr, nullptr, c, stream);
       else
         r = attn_checked(q, k, v, B, H, S, S, D, st, st, scale, lo, hi, false, last ? o : acc,
-                         last ? o_dtype : partial_dtype, st, lse, acc, partial_dtype, st, lse, defer, stream);
+                         last ? o_dtype : partial_dtype, st, lse, acc, partial_dtype, st, lse, c, stream);
     } else {
       r = attn_checked(q, k, v, B, H, S, S, D, st, st, scale, lo, hi, false,
                        static_cast<char *>(acc) + (size_t)c * part_o * psize, partial_dtype, st,
-                       lse_parts + (size_t)c * part_l, nullptr, DIT_BF16, nullptr, nullptr, defer, stream);
+                       lse_parts + (size_t)c * part_l, nullptr, DIT_BF16, nullptr, nullptr, c, stream);
     }
     if (r != DIT_OK) return r;  // the entry point has set the detail
   }

@@ -595,14 +595,6 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
                             bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
                             bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool defer_wait,
                             cudaStream_t stream, const char **detail) {
-  // D = 128: P in shared memory (variant 4), or non-causal CTA pairs (variants 2, 3); those
-  // kernels always wait for the previous launch at their start (defer_wait is a hint)
-  if (D == 128 && attention_variant() == 4)
-    return launch_attn_fwd_ps(q, k, v, B, H, Sq, Skv, q_st, kv_st, scale, kv_begin, kv_end, causal, o, o_f32, o_st,
-                              lse, o_acc, acc_f32, acc_st, lse_acc, stream, detail);
-  if (D == 128 && !causal && (attention_variant() == 2 || attention_variant() == 3))
-    return launch_attn_fwd_pair(q, k, v, B, H, Sq, Skv, q_st, kv_st, scale, kv_begin, kv_end, o, o_f32, o_st, lse,
-                                o_acc, acc_f32, acc_st, lse_acc, attention_variant() == 3, stream, detail);
   (void)Skv;
   CUtensorMap tq, tk, tv, to, tacc;
   const int n_kv = kv_end - kv_begin;

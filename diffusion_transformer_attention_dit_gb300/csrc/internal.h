@@ -14,10 +14,6 @@ namespace ditattn {
 // preamble overlap the previous kernel's tail).  Set by dit_set_launch_overlap.
 bool launch_overlap_enabled();
 
-// Attention kernel choice for D = 128 launches: 0 auto, 1 one CTA (P in TMEM), 2 CTA pairs, 3 CTA pairs
-// with one tile per CTA and three S buffers (2 and 3 non-causal only), 4 one CTA with P in shared memory.
-int attention_variant();
-
 // Set the text dit_last_error_detail returns (for entry points outside api.cu).
 void set_error_detail(const char *why);
 
@@ -37,27 +33,6 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// As launch_kernel, in clusters of cluster_x CTAs along x.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                                  unsigned cluster_x, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_x;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = launch_overlap_enabled() ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
 // Attention forward over keys [kv_begin, kv_end) (causal: query i sees keys j <= i).
 // Strides in elements {b, s, h}.  With o_acc non-null (update form) the result is
 // LSE-merged with the running (o_acc, lse_acc) before it is written.  defer_wait:
@@ -69,23 +44,6 @@ cudaError_t launch_attn_fwd(const void *q, const void *k, const void *v, int B, 
                             bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
                             bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool defer_wait,
                             cudaStream_t stream, const char **detail);
-
-// The same on CTA pairs (cta_group::2): D = 128, non-causal only.  one_tile: one
-// query tile per CTA with three S buffers; else two tiles per CTA.
-cudaError_t launch_attn_fwd_pair(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv,
-                                 const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
-                                 void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
-                                 bool acc_f32, const int64_t acc_st[3], const float *lse_acc, bool one_tile,
-                                 cudaStream_t stream, const char **detail);
-cudaError_t read_and_clear_pair_error(unsigned int *value);
-
-// The same with P in shared memory (S of the next block overlaps the softmax): D = 128.
-cudaError_t launch_attn_fwd_ps(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv,
-                               const int64_t q_st[3], const int64_t kv_st[3], float scale, int kv_begin, int kv_end,
-                               bool causal, void *o, bool o_f32, const int64_t o_st[3], float *lse, const void *o_acc,
-                               bool acc_f32, const int64_t acc_st[3], const float *lse_acc, cudaStream_t stream,
-                               const char **detail);
-cudaError_t read_and_clear_ps_error(unsigned int *value);
 
 cudaError_t launch_qk_norm_rope(const void *q, const void *k, void *q_out, void *k_out, const float *wq,
                                 const float *wk, const float *cos_tab, const float *sin_tab, int B, int S, int H,
@@ -123,12 +81,20 @@ cudaError_t read_and_clear_prologue_error(unsigned int *value);
 cudaError_t read_and_clear_merge_error(unsigned int *value);
 
 // The attention entry points' argument checks, then launch_attn_fwd (api.cu).
-// o_acc == nullptr: plain form; otherwise the update form.  defer_wait as above.
+// o_acc == nullptr: plain form; otherwise the update form.
+// sequence_chunk: the position of this launch in a sequence of attention chunk
+// launches that the caller issues back to back on `stream` (-1: not part of
+// one).  Only sequence_chunk >= 1 defers the dependency wait, and it is valid
+// only when the launch right before it on the stream is chunk sequence_chunk - 1
+// of the same sequence -- chunk 0 always waits for its predecessor (say a
+// prologue or a merge) at its start, and every deferred chunk waits for its
+// predecessor before it ends, so each chunk's start is ordered after whatever
+// preceded chunk 0.
 dit_status attn_checked(const void *q, const void *k, const void *v, int B, int H, int Sq, int Skv, int D,
                         const int64_t q_strides[3], const int64_t kv_strides[3], float scale, int kv_begin, int kv_end,
                         bool causal, void *o, dit_dtype o_dtype, const int64_t o_strides[3], float *lse,
                         const void *o_acc, dit_dtype acc_dtype, const int64_t acc_strides[3], const float *lse_acc,
-                        bool defer_wait, cudaStream_t stream);
+                        int sequence_chunk, cudaStream_t stream);
 
 // Attention over `chunks` equal KV chunks of contiguous bf16 BSHD q, k, v
 // (chunk c = keys [c*S/chunks, (c+1)*S/chunks)) and their merge, on `stream`

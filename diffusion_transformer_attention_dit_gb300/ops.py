@@ -22,7 +22,7 @@ EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
             "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace",
-            "dit_set_attention_variant", "dit_attention", "dit_attention_workspace", "dit_attention_noalloc")
+            "dit_attention", "dit_attention_workspace", "dit_attention_noalloc")
 
 _lib = None
 
@@ -60,10 +60,9 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
     lib.dit_set_launch_overlap.argtypes = [i32]
-    lib.dit_set_attention_variant.argtypes = [i32]
-    lib.dit_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, vp,
-                                       i32, vp, vp, ctypes.c_size_t, vp]
-    lib.dit_attention_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.dit_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, i32,
+                                       vp, i32, vp, vp, ctypes.c_size_t, vp]
+    lib.dit_attention_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
     lib.dit_attention_host_workspace.restype = ctypes.c_size_t
     lib.dit_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, i32, vp,
                                   i32, vp, vp, ctypes.c_size_t, vp, vp, vp]
@@ -74,7 +73,7 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
                  "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap",
-                 "dit_attention_host", "dit_set_attention_variant", "dit_attention", "dit_attention_noalloc"):
+                 "dit_attention_host", "dit_attention", "dit_attention_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -291,11 +290,6 @@ def set_launch_overlap(enable: bool):
     _check(load_library().dit_set_launch_overlap(1 if enable else 0))
 
 
-def set_attention_variant(variant: int):
-    """Attention kernel for head dim 128 without a mask: 0 default, 1 one CTA, 2 CTA pairs (cta_group::2)."""
-    _check(load_library().dit_set_attention_variant(int(variant)))
-
-
 def selftest_wait_timeout(stream=None):
     """Run the bounded-wait self-test kernel; a following poll_device_error() must raise DIT_ERR_TIMEOUT."""
     _check(load_library().dit_selftest_wait_timeout(_stream(stream)))
@@ -368,20 +362,27 @@ def dit_attention(q, k, v, wq, wk, cos, sin, eps: float = 1e-6, chunks: int = 1,
 
 
 def attention_host_workspace_bytes(B, S, H, D, chunks=1, prologue=True, partial_dtype=torch.float32,
-                                   out_dtype=torch.bfloat16) -> int:
+                                   out_dtype=torch.bfloat16, merge: str = "update") -> int:
     """Device workspace bytes dit_attention_host needs for these sizes."""
+    if merge not in ("kernel", "update"):
+        raise ValueError("merge must be 'kernel' or 'update'")
     return int(load_library().dit_attention_host_workspace(B, S, H, D, chunks, int(bool(prologue)),
-                                                           _dtype_code(partial_dtype), _dtype_code(out_dtype)))
+                                                           _dtype_code(partial_dtype), int(merge == "update"),
+                                                           _dtype_code(out_dtype)))
 
 
 def dit_attention_host(q, k, v, wq=None, wk=None, cos=None, sin=None, eps: float = 1e-6, chunks: int = 1,
                        scale: float | None = None, partial_dtype=torch.float32, out_dtype=torch.bfloat16,
-                       prologue: bool = True, o=None, lse=None, workspace=None, stream=None):
+                       prologue: bool = True, merge: str = "update", o=None, lse=None, workspace=None, stream=None):
     """The whole hot path from host tensors (pinned for asynchronous copies): q, k, v bf16 [B, S, H, D]; wq, wk
-    fp32 [D]; cos, sin fp32 [S, D/2].  The value rows of each KV chunk are copied while earlier chunks compute.
+    fp32 [D]; cos, sin fp32 [S, D/2].  merge="update": the value rows of each KV chunk are copied while earlier
+    chunks compute, later chunks merged into a running result in their epilogue.  merge="kernel": stacked partials
+    and the merge kernel over query-row ranges, each range's result copied back while the next computes.
     Returns host (o, lse); they are valid once the stream has completed the call, and the inputs must stay
     referenced until then (the copies read them asynchronously).  `workspace` is a device uint8 tensor of at
     least attention_host_workspace_bytes(...) bytes (allocated here when None)."""
+    if merge not in ("kernel", "update"):
+        raise ValueError("merge must be 'kernel' or 'update'")
     lib = load_library()
     for t in (q, k, v):
         if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous():
@@ -401,7 +402,7 @@ def dit_attention_host(q, k, v, wq=None, wk=None, cos=None, sin=None, eps: float
         lse = torch.empty((B, H, S), dtype=torch.float32, pin_memory=pin)
     if o.device.type != "cpu" or lse.device.type != "cpu" or not (o.is_contiguous() and lse.is_contiguous()):
         raise ValueError("o and lse must be contiguous host tensors")
-    need = attention_host_workspace_bytes(B, S, H, D, chunks, prologue, partial_dtype, o.dtype)
+    need = attention_host_workspace_bytes(B, S, H, D, chunks, prologue, partial_dtype, o.dtype, merge)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
         if stream is not None:  # the allocator must not hand the block out again before `stream` is done with it
@@ -411,9 +412,9 @@ def dit_attention_host(q, k, v, wq=None, wk=None, cos=None, sin=None, eps: float
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
     _check(lib.dit_attention_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(wq), ptr(wk), ptr(cos), ptr(sin),
                                   B, S, H, D, float(eps), float(scale), int(chunks), int(bool(prologue)),
-                                  _dtype_code(partial_dtype), o.data_ptr(), _dtype_code(o.dtype), lse.data_ptr(),
-                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                  _stream(stream)))
+                                  _dtype_code(partial_dtype), int(merge == "update"), o.data_ptr(),
+                                  _dtype_code(o.dtype), lse.data_ptr(), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
     return o, lse
 
 

@@ -285,21 +285,33 @@ dit_status dit_gemm_fp8(const void *a, const float *a_scale, const void *b, cons
 /*
  * dit_attention_host -- the whole hot path (prologue, attention over `chunks`
  * equal KV chunks, LSE merge) on inputs in host memory, results back in host
- * memory.
+ * memory, with the copies pipelined against the kernels.
  *
- * Copies q, k (and, with the prologue, wq, wk, cos_tab, sin_tab) into the
- * device workspace on an internal copy stream, then the value rows of each KV
- * chunk in turn; on `stream` it runs dit_qk_norm_rope in place, dit_attn_fwd
- * over chunk 0 (into a running result of partial_dtype, or straight into the
- * output when chunks == 1) and dit_attn_fwd_update over every later chunk (the
- * last one writing the output), each attention waiting only for its own value
- * rows, and finally copies O and LSE to the host.  Chunk c covers keys
- * [c*S/chunks, (c+1)*S/chunks).  Same operations and results as calling those
- * entry points on device copies of the inputs.
+ * Chunk c covers keys [c*S/chunks, (c+1)*S/chunks).  The copies run on two
+ * streams the call creates (inputs, outputs) and releases once their work is
+ * done; the kernels run on `stream`.
+ *   merge_update = 1 (and chunks > 1): q and k (with the prologue also wq, wk,
+ *     cos_tab, sin_tab) are copied in, then the value rows of each chunk in
+ *     turn (without the prologue each chunk's key rows travel with its value
+ *     rows); dit_qk_norm_rope runs in place, dit_attn_fwd over chunk 0 into a
+ *     running result of partial_dtype, and dit_attn_fwd_update over every
+ *     later chunk, each waiting only for its own rows; O and LSE are copied
+ *     back at the end.
+ *   merge_update = 0, or chunks == 1: the query rows are processed in up to 8
+ *     ranges whose edges are multiples of 256 rows (fewer ranges when a range
+ *     would hold fewer than 608 query tiles of 256 rows over all (b, h)).  Per
+ *     range: dit_attn_fwd over every chunk into stacked partials of
+ *     partial_dtype, dit_attn_merge_lse (chunks > 1), and the range's O and
+ *     LSE copied back while the next range computes.  Without the prologue the
+ *     inputs arrive as: the first range's query rows, each chunk's key and
+ *     value rows, the other ranges' query rows; with it, q and k in full first.
+ * Results are bit-identical to dit_attention with the same chunks,
+ * merge_update and partial_dtype on device copies of the inputs.
  *
  * Defined by: the entry points it composes (see each); the chunk-by-chunk
  * combination is the ring step of "feat: support Ascend NPU backend (torch_npu)
- * for Qwen-Image pipelines - #274", item 2.
+ * for Qwen-Image pipelines - #274", item 2, the stacked merge the LSE merge of
+ * its sequence-parallel paths.
  *
  *   q, k, v          host bf16 [B, S, H, D], contiguous (pinned memory lets the
  *                    copies run asynchronously); must stay valid until `stream`
@@ -309,21 +321,24 @@ dit_status dit_gemm_fp8(const void *a, const float *a_scale, const void *b, cons
  *   eps, scale       as for dit_qk_norm_rope / dit_attn_fwd
  *   chunks           1 <= chunks <= S
  *   prologue         1: QK-RMSNorm + RoPE first; 0: attention on q, k as given
- *   partial_dtype    dtype of the running result between chunks
+ *   partial_dtype    dtype of the running result / stacked partials
+ *   merge_update     1: running result merged in each later chunk's epilogue;
+ *                    0: stacked partials and the merge kernel, per query range
  *   o, o_dtype       host [B, S, H, D] output; lse host fp32 [B, H, S]
  *   workspace        device memory of at least dit_attention_host_workspace(...)
  *                    bytes, 256-byte aligned, owned by the caller; it must not be
  *                    used by other work until `stream` has passed this call
  * Asynchronous on `stream`: o and lse are valid once `stream` has completed the
  * call.  Errors as for the composed entry points; a workspace that is too small
- * or misaligned is DIT_ERR_INVALID_ARG.
+ * or misaligned is DIT_ERR_INVALID_ARG; a chunk count the merge kernel cannot
+ * take (merge_update = 0) is DIT_ERR_UNSUPPORTED before anything is queued.
  */
 size_t dit_attention_host_workspace(int B, int S, int H, int D, int chunks, int prologue,
-                                    dit_dtype partial_dtype, dit_dtype o_dtype);
+                                    dit_dtype partial_dtype, int merge_update, dit_dtype o_dtype);
 dit_status dit_attention_host(const void *q, const void *k, const void *v,
                               const float *wq, const float *wk, const float *cos_tab, const float *sin_tab,
                               int B, int S, int H, int D, float eps, float scale, int chunks, int prologue,
-                              dit_dtype partial_dtype, void *o, dit_dtype o_dtype, float *lse,
+                              dit_dtype partial_dtype, int merge_update, void *o, dit_dtype o_dtype, float *lse,
                               void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
@@ -391,12 +406,18 @@ dit_status dit_attention(const void *q, const void *k, const void *v,
  *   limit            the scratch holds 32 MiB: sizes whose
  *                    dit_attention_workspace(...) is larger are refused with
  *                    DIT_ERR_UNSUPPORTED before anything is launched
- * The first call on a device brings the 32 MiB scratch onto that device (the
- * CUDA runtime loads a library's device data on first use) and looks up its
- * device address, with that device current; the memory stays reserved until
- * the process exits.  Make that first call before any stream capture.  All calls share the scratch: nothing in it needs to start at
- * zero, but calls that run concurrently on the GPU (other streams, other host
- * threads) race on it.  Allocates nothing.  Errors as for dit_attention.
+ * Residency: with the CUDA runtime's default lazy module loading, the first
+ * call on a device brings the 32 MiB scratch onto that device, and it stays
+ * reserved until the process exits; with CUDA_MODULE_LOADING=EAGER the scratch
+ * is reserved on every device where the process creates a context, as soon as
+ * the library is loaded, even if this entry point is never called.  Every call
+ * looks the scratch's device address up afresh (cudaGetSymbolAddress with the
+ * call's device current), so a context rebuilt after cudaDeviceReset gets the
+ * right address.  The first call on a device may load the library's module
+ * there: make it before any stream capture.  All calls share the scratch:
+ * nothing in it needs to start at zero, but calls that run concurrently on
+ * the GPU (other streams, other host threads) race on it.  Allocates nothing.
+ * Errors as for dit_attention.
  */
 dit_status dit_attention_noalloc(const void *q, const void *k, const void *v,
                                  const float *wq, const float *wk, const float *cos_tab, const float *sin_tab,
@@ -433,20 +454,6 @@ dit_status dit_selftest_wait_timeout(struct CUstream_st *stream);
  * Returns DIT_ERR_INVALID_ARG for any other value.
  */
 dit_status dit_set_launch_overlap(int enable);
-
-/*
- * dit_set_attention_variant -- which attention kernel serves head dim 128
- * without a causal mask (dit_attn_fwd, dit_attn_fwd_update, dit_attention_host):
- * 0 = the library's default, 1 = one CTA per 256 query rows, 2 = CTA pairs
- * (clusters of 2 running M = 256 tcgen05 MMAs, each SM holding half of every
- * K/V block), 3 = CTA pairs with one query tile per CTA and S computed three
- * blocks ahead, 4 = one CTA per 256 rows with P kept in shared memory (S of the
- * next block computed while the softmax runs; also serves causal calls).
- * Variants 2 and 3 serve only the non-causal calls (causal ones use the
- * default).  Results agree to floating-point rounding; all are tested.
- * Process-wide; DIT_ERR_INVALID_ARG for any other value.
- */
-dit_status dit_set_attention_variant(int variant);
 
 /* dit_status_string -- static, human-readable name of a status code (never NULL). */
 const char *dit_status_string(dit_status s);

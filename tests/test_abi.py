@@ -198,24 +198,37 @@ def test_launch_overlap_setting(lib):
 
 def _host(lib, **kw):
     B, S, H, D = kw.pop("B", 1), kw.pop("S", 64), kw.pop("H", 2), kw.pop("D", 128)
-    chunks, prologue = kw.pop("chunks", 2), kw.pop("prologue", 1)
-    need = lib.dit_attention_host_workspace(B, S, H, D, chunks, 1, 1, 0)
+    chunks, prologue, mu = kw.pop("chunks", 2), kw.pop("prologue", 1), kw.pop("merge_update", 1)
+    need = lib.dit_attention_host_workspace(B, S, H, D, chunks, 1, 1, 1 if mu not in (0, 1) else mu, 0)
     a = dict(q=A16, k=A16 * 2, v=A16 * 3, wq=A16 * 4, wk=A16 * 5, cos=A16 * 6, sin=A16 * 7, o=A16 * 8, lse=A16 * 9,
              ws=A16 * 16, wsb=need, pdt=1, odt=0)
     a.update(kw)
     return lib.dit_attention_host(a["q"], a["k"], a["v"], a["wq"], a["wk"], a["cos"], a["sin"], B, S, H, D, 1e-6,
-                                  0.088, chunks, prologue, a["pdt"], a["o"], a["odt"], a["lse"], a["ws"], a["wsb"],
-                                  None)
+                                  0.088, chunks, prologue, a["pdt"], mu, a["o"], a["odt"], a["lse"], a["ws"],
+                                  a["wsb"], None)
 
 
 def test_host_workspace_size(lib):
     B, S, H, D = 2, 100, 3, 128
     act = B * S * H * D * 2
-    n = lib.dit_attention_host_workspace(B, S, H, D, 2, 1, 1, 0)
+    n = lib.dit_attention_host_workspace(B, S, H, D, 2, 1, 1, 1, 0)
     # q, k, v, an fp32 running result, a bf16 output, LSE, tables: at least their sum
     assert n >= 3 * act + 2 * act + act + B * H * S * 4 + 2 * S * (D // 2) * 4
-    assert lib.dit_attention_host_workspace(B, S, H, D, 1, 0, 1, 0) < n  # no running result, no tables
-    assert lib.dit_attention_host_workspace(B, S, H, D, 0, 1, 1, 0) == 0
+    assert lib.dit_attention_host_workspace(B, S, H, D, 1, 0, 1, 1, 0) < n  # no running result, no tables
+    assert lib.dit_attention_host_workspace(B, S, H, D, 0, 1, 1, 1, 0) == 0
+    # stacked partials (one query range at this size): q, k, v, C fp32 parts and their LSEs, two output stages
+    m = lib.dit_attention_host_workspace(B, S, H, D, 3, 0, 1, 0, 0)
+    assert m >= 3 * act + 3 * 2 * act + 3 * B * H * S * 4 + 2 * (act + B * H * S * 4)
+
+
+def test_host_workspace_query_ranges(lib):
+    """Stacked partials over query ranges: the partial buffers hold one range (at most ceil(S/8) rounded up to
+    256 rows plus the ragged last range), not the whole sequence."""
+    B, S, H, D, C = 1, 75600, 40, 128, 8
+    act = B * S * H * D * 2
+    n = lib.dit_attention_host_workspace(B, S, H, D, C, 0, 0, 0, 0)
+    whole = 3 * act + C * act  # q, k, v and every chunk's full-length bf16 partial
+    assert 3 * act + C * act // 8 < n < whole
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -228,6 +241,8 @@ def test_host_workspace_size(lib):
     (dict(ws=A16 * 16 + 128), ops.DIT_ERR_INVALID_ARG),   # workspace not 256-byte aligned
     (dict(wsb=1024), ops.DIT_ERR_INVALID_ARG),            # workspace too small
     (dict(pdt=5), ops.DIT_ERR_INVALID_ARG),
+    (dict(merge_update=2), ops.DIT_ERR_INVALID_ARG),
+    (dict(merge_update=0, S=2048, chunks=1100, wsb=1 << 40), ops.DIT_ERR_UNSUPPORTED),  # > the merge's part limit
 ])
 def test_host_path_rejects_bad_arguments(lib, kw, code):
     assert _host(lib, **kw) == code
@@ -236,13 +251,6 @@ def test_host_path_rejects_bad_arguments(lib, kw, code):
 
 def test_host_path_empty_work_is_ok(lib):
     assert _host(lib, B=0) == ops.DIT_OK
-
-
-def test_attention_variant_setting(lib):
-    assert lib.dit_set_attention_variant(5) == ops.DIT_ERR_INVALID_ARG
-    assert lib.dit_set_attention_variant(-1) == ops.DIT_ERR_INVALID_ARG
-    for v in (4, 3, 2, 1, 0):
-        assert lib.dit_set_attention_variant(v) == ops.DIT_OK
 
 
 def _device_path(lib, **kw):

@@ -35,23 +35,9 @@ def _device_compare(a: torch.Tensor, b: torch.Tensor):
     return err, cos
 
 
-@pytest.mark.parametrize("name,merge,variant", [("qwen_image", "update", 0), ("qwen_image", "kernel", 0),
-                                                ("qwen_image_edit", "update", 0), ("wan480", "kernel", 0),
-                                                ("wan720", "kernel", 0), ("qwen_image", "update", 2),
-                                                ("wan480", "kernel", 2), ("qwen_image", "update", 3),
-                                                ("wan480", "kernel", 3), ("qwen_image", "update", 4),
-                                                ("wan480", "kernel", 4), ("wan720", "kernel", 4)])
-def test_workload_parity(name, merge, variant):
-    """variant: the attention kernel for head dim 128 (0 the default, 2 and 3 the CTA-pair kernels, 4 P in
-    shared memory)."""
-    ops.set_attention_variant(variant)
-    try:
-        _workload_parity(name, merge)
-    finally:
-        ops.set_attention_variant(0)
-
-
-def _workload_parity(name, merge):
+@pytest.mark.parametrize("name,merge", [("qwen_image", "update"), ("qwen_image", "kernel"),
+                                        ("qwen_image_edit", "update"), ("wan480", "kernel"), ("wan720", "kernel")])
+def test_workload_parity(name, merge):
     orc = oracle.get()
     inp = inputs.make_inputs(name)
     w = inp.w
