@@ -53,14 +53,15 @@ cudaError_t launch_merge_lse(const void *o_parts, bool in_f32, const float *lse_
                              int D, int64_t part_stride_o, int64_t part_stride_lse, void *o, bool out_f32,
                              float *lse, cudaStream_t stream);
 
-// Row normalisations (LayerNorm + adaLN modulation; RMSNorm over C).  C % 8 == 0, C <= row_norm_max_channels().
+// Row normalisations (row_kernels.cu): LayerNorm + adaLN modulation, RMSNorm over C.
+// C % 8 == 0, C <= row_norm_max_channels().
 int row_norm_max_channels();
 cudaError_t launch_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y, int B, int L,
                                        int C, float eps, cudaStream_t stream);
 cudaError_t launch_rms_norm(const void *x, const float *w, void *y, long long rows, int C, float eps,
                             cudaStream_t stream);
 
-// W8A8 fp8: per-row dynamic quantisation (K % 8 == 0, K <= quant_fp8_max_k()) and the scaled GEMM.
+// W8A8 fp8 (fp8.cu): per-row dynamic quantisation (K % 8 == 0, K <= quant_fp8_max_k()) and the scaled GEMM.
 int quant_fp8_max_k();
 cudaError_t launch_quant_fp8_rows(const void *x, void *codes, float *scale, long long M, int K, cudaStream_t stream);
 cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, const float *b_scale, void *out,

@@ -1,0 +1,247 @@
+// Row kernels of a DiT block on GB300 (sm_103a): LayerNorm with adaLN
+// modulation, and RMSNorm over all C channels of a token.
+//
+// LayerNorm-modulate ("NPU Wan2.2-I2V model inference optimisation practice",
+// section "NPU layer_norm_eval operator adaptation": WanLayerNorm without
+// affine parameters, and FusedLayerNormModulate passing 1 + scale as the
+// weight and shift as the bias of one layer-norm call), per row x of C:
+//   y = (x - mean) / sqrt(var + eps) * (1 + scale[b]) + shift[b]   (biased var)
+// RMSNorm over C (same page, section "NPU rms_norm operator adaptation":
+// WanRMSNorm on [B, L, C]):   y = x * w / sqrt(mean(x^2) + eps)
+// fp32 arithmetic, one bf16 rounding.
+//
+// HBM-bound (a read and a write per element).  A row is spread over 128
+// threads as 16-byte vectors held in registers as loaded (C <= 8192, C a
+// multiple of 8) and read from HBM once; persistent CTAs issue the next row's
+// loads before reducing the current one.  Each kernel reduces once per row:
+// the sums of (x - K) and (x - K)^2 with K the row's first element (the
+// shifted-data form of the variance, which avoids the cancellation of
+// E[x^2] - mean^2 when |mean| >> std), or the sum of squares; one barrier per
+// row.  The arithmetic runs on pairs of channels in the packed fp32 pipes
+// (FADD2 / FFMA2 / FMUL2), which cut LayerNorm-modulate from 0.74 to 0.84 of
+// the measured HBM bandwidth at the Wan2.2 720p shape.  (Also measured on
+// GB300 and slower: deeper prefetch -- three or four rows per CTA in
+// registers, or a ring of rows in shared memory filled by cp.async or by bulk
+// copies -- one warp per row, and fewer CTAs per SM.)
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn_math.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace ditattn {
+namespace {
+
+using attn::f2;
+using attn::f2_add;
+using attn::f2_fma;
+using attn::f2_mul;
+using attn::f2_split;
+
+enum Mode { kLayerNormModulate = 0, kRmsNorm = 1 };
+
+constexpr int kThreads = 128;
+constexpr int kMaxVec = 8;  // 16-byte vectors per thread: C <= 8 * 8 * 128 = 8192
+constexpr int kMaxCtasPerSm = 8;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// The two bf16 channels of one 32-bit word as a packed fp32 pair.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Sums over the CTA; every thread gets the results.  `red` holds 8 floats.  One
+// barrier per call: the callers alternate between two `red` buffers, and the
+// barrier of the next call on the other buffer orders each buffer's reads
+// before its next writes.
+__device__ __forceinline__ float2 block_reduce2(float v, float w, float *red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    v += __shfl_xor_sync(0xffffffffu, v, off);
+    w += __shfl_xor_sync(0xffffffffu, w, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = v;
+    red[4 + (threadIdx.x >> 5)] = w;
+  }
+  __syncthreads();
+  return make_float2((red[0] + red[1]) + (red[2] + red[3]), (red[4] + red[5]) + (red[6] + red[7]));
+}
+
+// Eight consecutive fp32 (32-byte aligned) as four packed pairs.
+__device__ __forceinline__ void load_f2x4(const float *p, uint64_t (&f)[4]) {
+  const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p));
+  const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  f[0] = f2(a0.x, a0.y), f[1] = f2(a0.z, a0.w), f[2] = f2(a1.x, a1.y), f[3] = f2(a1.z, a1.w);
+}
+
+// One row whose 16-byte vectors this thread holds in `raw` (kLayerNormModulate:
+// a = scale [B, C], c = shift [B, C], either may be null, L rows per batch
+// entry; kRmsNorm: a = weight [C]).
+template <int kMode, int kVec>
+__device__ __forceinline__ void process_row(const uint4 (&raw)[kVec], uint32_t first, uint8_t *y, const float *a,
+                                            const float *c, long long r, int nvec, int C, int L,
+                                            float eps, float *red) {
+  const float inv_c = 1.0f / C;
+  // pass 1: this thread's part of the reduction, on channel pairs
+  uint64_t s2 = 0ull, ss2 = 0ull;  // (0.0f, 0.0f)
+  const float K = __uint_as_float(first << 16);
+  const uint64_t negk2 = f2(-K, -K);
+#pragma unroll
+  for (int u = 0; u < kVec; ++u)
+    if (threadIdx.x + u * kThreads < nvec) {
+      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint64_t v2 = bf16x2_to_f2(w[e]);
+        if (kMode == kLayerNormModulate) {
+          const uint64_t d2 = f2_add(v2, negk2);
+          s2 = f2_add(s2, d2);
+          ss2 = f2_fma(d2, d2, ss2);
+        } else {
+          ss2 = f2_fma(v2, v2, ss2);
+        }
+      }
+    }
+  float s0, s1, q0, q1;
+  f2_split(s2, s0, s1);
+  f2_split(ss2, q0, q1);
+  const float2 tot = block_reduce2(s0 + s1, q0 + q1, red);
+
+  // pass 2: the outputs
+  uint64_t neg_mu2, inv2;
+  if (kMode == kLayerNormModulate) {
+    const float dm = tot.x * inv_c;  // mean - K
+    const float mu = K + dm, inv = rsqrtf(fmaxf(fmaf(tot.y, inv_c, -dm * dm), 0.f) + eps);
+    neg_mu2 = f2(-mu, -mu);
+    inv2 = f2(inv, inv);
+  } else {
+    const float inv = rsqrtf(fmaf(tot.y, inv_c, eps));
+    neg_mu2 = 0ull;
+    inv2 = f2(inv, inv);
+  }
+  const long long frow = kMode == kLayerNormModulate ? (r / L) * C : 0;
+  uint4 *yv = reinterpret_cast<uint4 *>(y) + r * nvec;
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    if (i < nvec) {
+      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+      uint64_t fa[4] = {0ull, 0ull, 0ull, 0ull}, fc[4] = {0ull, 0ull, 0ull, 0ull};
+      if (a) load_f2x4(a + frow + 8 * i, fa);
+      if (kMode == kLayerNormModulate && c) load_f2x4(c + frow + 8 * i, fc);
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint64_t v2 = bf16x2_to_f2(w[e]);
+        uint64_t y2;
+        if (kMode == kLayerNormModulate) {
+          // (x - mu) * (inv * (1 + scale)) + shift; a missing scale or shift reads as zeros
+          const uint64_t g2 = f2_fma(inv2, fa[e], inv2);
+          y2 = f2_fma(f2_add(v2, neg_mu2), g2, fc[e]);
+        } else {
+          y2 = f2_mul(f2_mul(v2, inv2), fa[e]);
+        }
+        float lo, hi;
+        f2_split(y2, lo, hi);
+        o[e] = pack_bf16x2(lo, hi);
+      }
+      __stcs(yv + i, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+}
+
+template <int kVec>
+__device__ __forceinline__ void load_row(uint4 (&raw)[kVec], uint32_t &first, const uint4 *__restrict__ x,
+                                         long long r, int nvec) {
+#pragma unroll
+  for (int u = 0; u < kVec; ++u) {
+    const int i = threadIdx.x + u * kThreads;
+    if (i < nvec) raw[u] = __ldcs(x + r * nvec + i);
+  }
+  // the row's first element (LayerNorm's shift), one broadcast load per warp
+  first = __ldg(reinterpret_cast<const unsigned int *>(x + r * nvec));
+}
+
+// Persistent CTAs walk rows r = blockIdx.x, + gridDim.x, ...; the next row's
+// loads are issued before the current row's reduction, so two rows per CTA
+// are in flight.  One barrier per row: consecutive rows alternate between
+// red[0..7] and red[8..15].
+template <int kMode, int kVec>
+__global__ void __launch_bounds__(kThreads) row_kernel(const uint4 *__restrict__ x, uint8_t *y,
+                                                       const float *__restrict__ a, const float *__restrict__ c,
+                                                       long long rows, int C, int L, float eps) {
+  __shared__ float red[16];
+  const int nvec = C / 8;
+  uint4 cur[kVec], nxt[kVec];
+  uint32_t fcur = 0, fnxt = 0;
+  griddep_wait();
+  griddep_launch_dependents();
+  long long r = blockIdx.x;
+  if (r < rows) load_row<kVec>(cur, fcur, x, r, nvec);
+  for (; r < rows; r += 2LL * gridDim.x) {
+    const long long r1 = r + gridDim.x;
+    if (r1 < rows) load_row<kVec>(nxt, fnxt, x, r1, nvec);
+    process_row<kMode, kVec>(cur, fcur, y, a, c, r, nvec, C, L, eps, red);
+    if (r1 >= rows) break;
+    const long long r2 = r1 + gridDim.x;
+    if (r2 < rows) load_row<kVec>(cur, fcur, x, r2, nvec);
+    process_row<kMode, kVec>(nxt, fnxt, y, a, c, r1, nvec, C, L, eps, red + 8);
+  }
+}
+
+// Persistent grid: as many CTAs as can be resident (registers decide, since a
+// thread holds kVec row vectors twice), capped at 8 per SM.
+template <int kMode, int kVec>
+cudaError_t launch_vec(const void *x, void *y, const float *a, const float *c, long long rows, int C,
+                       int L, float eps, cudaStream_t stream) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_kernel<kMode, kVec>, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  const long long cap = (long long)(per_sm < 1 ? 1 : per_sm > kMaxCtasPerSm ? kMaxCtasPerSm : per_sm) * sms;
+  const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
+  return launch_kernel(row_kernel<kMode, kVec>, dim3(grid), dim3(kThreads), 0, stream,
+                       static_cast<const uint4 *>(x), static_cast<uint8_t *>(y), a, c, rows, C, L, eps);
+}
+
+// kVec = the number of 16-byte vectors each of the 128 threads holds: exactly
+// ceil(C / 8 / 128), so no registers go to vectors past the row's end.
+template <int kMode>
+cudaError_t launch(const void *x, void *y, const float *a, const float *c, long long rows, int C,
+                   int L, float eps, cudaStream_t stream) {
+  switch ((C / 8 + kThreads - 1) / kThreads) {
+    case 1: return launch_vec<kMode, 1>(x, y, a, c, rows, C, L, eps, stream);
+    case 2: return launch_vec<kMode, 2>(x, y, a, c, rows, C, L, eps, stream);
+    case 3: return launch_vec<kMode, 3>(x, y, a, c, rows, C, L, eps, stream);
+    case 4: return launch_vec<kMode, 4>(x, y, a, c, rows, C, L, eps, stream);
+    case 5: return launch_vec<kMode, 5>(x, y, a, c, rows, C, L, eps, stream);
+    case 6: return launch_vec<kMode, 6>(x, y, a, c, rows, C, L, eps, stream);
+    case 7: return launch_vec<kMode, 7>(x, y, a, c, rows, C, L, eps, stream);
+    default: return launch_vec<kMode, kMaxVec>(x, y, a, c, rows, C, L, eps, stream);
+  }
+}
+
+}  // namespace
+
+int row_norm_max_channels() { return kMaxVec * 8 * kThreads; }
+
+cudaError_t launch_layer_norm_modulate(const void *x, const float *scale, const float *shift, void *y, int B, int L,
+                                       int C, float eps, cudaStream_t stream) {
+  return launch<kLayerNormModulate>(x, y, scale, shift, (long long)B * L, C, L, eps, stream);
+}
+
+cudaError_t launch_rms_norm(const void *x, const float *w, void *y, long long rows, int C, float eps,
+                            cudaStream_t stream) {
+  return launch<kRmsNorm>(x, y, w, nullptr, rows, C, 1, eps, stream);
+}
+
+}  // namespace ditattn
