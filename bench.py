@@ -62,7 +62,9 @@ MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", 
 PER_WORKLOAD = ("qwen_image", "qwen_image_edit", "wan480")
 # DRAM bytes (read + write) per attention launch, from an ncu capture of the attention source with this sha256
 # prefix; reported as roofline.traffic only while the source is unchanged.
-ATTN_TRAFFIC = {"source_sha256_prefix": None, "by_workload": {}, "capture": ""}
+ATTN_TRAFFIC = {"source_sha256_prefix": "f32b5f4f04251cb4", "by_workload": {"wan720": 1717.2e6},
+                "capture": "stored ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of one Wan2.2-720p "
+                           "chunk launch, bench.py --profile-kernel attention --workload wan720"}
 
 
 def peaks():
@@ -779,6 +781,61 @@ def run_hbm_kernels(args):
                       "kernels": res}))
 
 
+def run_profile_kernel(args):
+    """Diagnostic for ncu captures: exactly three launches of one kernel at the workload's shapes (synthetic
+    inputs; --profile-heads shrinks H to keep the device footprint of a multi-pass capture at a few GB).  The
+    attention runs the second of the workload's KV chunks, as a bench step does."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import build, ops
+
+    build.build()
+    ops.load_library()
+    w = inputs.WORKLOADS[args.workload]
+    B, S, D = w.B, w.S, w.D
+    H = args.profile_heads or w.H
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321 + w.index)
+    rnd = lambda *shape: torch.randn(*shape, device=dev, generator=g)  # noqa: E731
+    kind = args.profile_kernel
+    if kind in ("prologue", "attention"):
+        q, k = rnd(B, S, H, D).to(torch.bfloat16), (w.k_scale * rnd(B, S, H, D)).to(torch.bfloat16)
+    if kind == "prologue":
+        wq, wk, cos, sin = 1 + 0.1 * rnd(D), 1 + 0.1 * rnd(D), rnd(S, D // 2), rnd(S, D // 2)
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        run = lambda: ops.qk_norm_rope(q, k, wq, wk, cos, sin, w.eps, q_out=qo, k_out=ko)  # noqa: E731
+    elif kind == "attention":
+        v = rnd(B, S, H, D).to(torch.bfloat16)
+        lo, hi = w.chunk_bounds(max(w.chunks, 2))[1]
+        o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        run = lambda: ops.attn_fwd(q, k, v, None, lo, hi, o=o, lse=lse)  # noqa: E731
+    elif kind == "merge":
+        C = max(w.chunks, 2)
+        parts = rnd(C, B, S, H, D).to(torch.float32 if PARTIAL[w.name] == "f32" else torch.bfloat16)
+        lp = 3 + 2 * rnd(C, B, H, S)
+        o, lse = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev), torch.empty((B, H, S), device=dev)
+        run = lambda: ops.attn_merge_lse(parts, lp, o=o, lse=lse)  # noqa: E731
+    else:
+        x = rnd(B, S, H * D).to(torch.bfloat16)
+        y = torch.empty_like(x)
+        if kind == "layer_norm_modulate":
+            sc, sh = 0.1 * rnd(B, H * D), 0.1 * rnd(B, H * D)
+            run = lambda: ops.layer_norm_modulate(x, sc, sh, w.eps, y=y)  # noqa: E731
+        elif kind == "rms_norm":
+            wn = 1 + 0.1 * rnd(H * D)
+            run = lambda: ops.rms_norm(x, wn, w.eps, y=y)  # noqa: E731
+        else:
+            codes = torch.empty((B * S, H * D), dtype=torch.uint8, device=dev)
+            scales = torch.empty(B * S, dtype=torch.float32, device=dev)
+            run = lambda: ops.quant_fp8_rows(x.view(B * S, H * D), codes, scales)  # noqa: E731
+    for _ in range(3):
+        run()
+    ops.poll_device_error()
+    print(json.dumps({"mode": "profile_kernel", "kernel": kind, "workload": w.name, "H": H, "launches": 3}))
+
+
 def run_qkv_fp8(args):
     """Diagnostic: per-token e4m3 quantisation of the tokens (B*S x H*D) and the fp8 GEMM with a
     [3*H*D, H*D] QKV weight, synthetic, timed with CUDA events (L2 flushed before each step)."""
@@ -842,6 +899,10 @@ def main():
                     help="time each HBM-bound kernel alone at the workload's shapes instead (diagnostic)")
     ap.add_argument("--qkv-fp8", action="store_true",
                     help="time the W8A8 fp8 QKV projection of the workload's tokens instead (diagnostic)")
+    ap.add_argument("--profile-kernel", default=None,
+                    choices=["prologue", "attention", "merge", "layer_norm_modulate", "rms_norm", "quant_fp8"],
+                    help="run exactly three launches of one kernel at the workload's shapes (for ncu captures)")
+    ap.add_argument("--profile-heads", type=int, default=0, help="heads for --profile-kernel (0: the workload's)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per attention launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -855,6 +916,8 @@ def main():
         run_ring_overlap(args)
     elif args.qkv_fp8:
         run_qkv_fp8(args)
+    elif args.profile_kernel:
+        run_profile_kernel(args)
     elif args.hbm_kernels:
         run_hbm_kernels(args)
     else:

@@ -11,10 +11,14 @@ rotary_mul operator adaptation") likewise takes precomputed cos/sin tensors.
 Workloads (shapes of the DiT models the pages discuss; all tensors synthetic):
 
   tiny             B1 H2  D64  S256, 1-D positions, KV in 4 chunks
-  qwen_image       B1 H24 D128 S4312 = 256 text + 78x52 image tokens
-  qwen_image_edit  B2 H24 D128 S8624 = 512 text + 2 x 78x52 (target+reference)
-  wan480           B1 H40 D128 S32760 = 21x30x52 video patches
+  qwen_image       B1 H24 D128 S4312 = 256 text + 78x52 image tokens, one pass
+  qwen_image_edit  B2 H24 D128 S8624 = 512 text + 2 x 78x52 (target+reference), one pass
+  wan480           B1 H40 D128 S32760 = 21x30x52 video patches, one pass
   wan720           B1 H40 D128 S75600 = 21x45x80, K x 3, no prologue, 8 chunks
+
+Only the tiny and the 720p workloads are stated with a KV chunking; the
+others are single-pass attention (chunked runs of them take an explicit
+chunk count).
 
 Seeds: 1000*workload_index + 100*batch_index + tensor_id with tensor ids
 q=0, k=1, v=2, wq=3, wk=4.  Large tensors are drawn in fixed 4 Mi-element
@@ -74,9 +78,9 @@ WORKLOADS = {
     for w in [
         Workload(1, "tiny", 1, 2, 64, 256, 0, ((1, 1, 256),), (64,), 4, True,
                  description="tiny oracle case B1 H2 D64 S256, 1-D RoPE, 4 KV chunks"),
-        Workload(2, "qwen_image", 1, 24, 128, 4312, 256, ((1, 78, 52),), (16, 56, 56), 2, True,
+        Workload(2, "qwen_image", 1, 24, 128, 4312, 256, ((1, 78, 52),), (16, 56, 56), 1, True,
                  description="Qwen-Image joint attention B1 H24 D128 S4312 (256 text + 78x52 image)"),
-        Workload(3, "qwen_image_edit", 2, 24, 128, 8624, 512, ((1, 78, 52), (1, 78, 52)), (16, 56, 56), 2,
+        Workload(3, "qwen_image_edit", 2, 24, 128, 8624, 512, ((1, 78, 52), (1, 78, 52)), (16, 56, 56), 1,
                  True, description="Qwen-Image-Edit B2 (CFG pair) H24 D128 S8624 (512 text + 2x78x52)"),
         Workload(4, "wan480", 1, 40, 128, 32760, 0, ((21, 30, 52),), (44, 42, 42), 1, True,
                  description="Wan2.2 480p video attention B1 H40 D128 S32760 (21x30x52)"),

@@ -17,8 +17,6 @@ pytestmark = pytest.mark.gpu
 
 PARTIAL = {"qwen_image": torch.float32, "qwen_image_edit": torch.float32, "wan480": torch.float32,
            "wan720": torch.bfloat16}
-# how bench.py combines the KV chunks of each workload (update: LSE merge in the attention epilogue)
-MERGE = {"qwen_image": "update", "qwen_image_edit": "update", "wan480": "kernel", "wan720": "kernel"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,15 +33,18 @@ def _device_compare(a: torch.Tensor, b: torch.Tensor):
     return err, cos
 
 
-@pytest.mark.parametrize("name,merge", [("qwen_image", "update"), ("qwen_image", "kernel"),
-                                        ("qwen_image_edit", "update"), ("wan480", "kernel"), ("wan720", "kernel")])
-def test_workload_parity(name, merge):
+@pytest.mark.parametrize("name,chunks,merge", [
+    ("qwen_image", 1, "kernel"), ("qwen_image_edit", 1, "kernel"), ("wan480", 1, "kernel"),  # as bench.py runs them
+    ("wan720", 8, "kernel"),
+    # the two-chunk forms (a local and a remote part, as in the Wan2.2 ring-overlap split), both merges
+    ("qwen_image", 2, "update"), ("qwen_image", 2, "kernel"), ("qwen_image_edit", 2, "update")])
+def test_workload_parity(name, chunks, merge):
     orc = oracle.get()
     inp = inputs.make_inputs(name)
     w = inp.w
     dq, dk, dv = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
     tabs = (dev_f32(inp.wq), dev_f32(inp.wk), dev_f32(inp.cos), dev_f32(inp.sin))
-    o, lse = ops.dit_attention(dq, dk, dv, *tabs, eps=w.eps, chunks=w.chunks, partial_dtype=PARTIAL[name],
+    o, lse = ops.dit_attention(dq, dk, dv, *tabs, eps=w.eps, chunks=chunks, partial_dtype=PARTIAL[name],
                                prologue=w.prologue, merge=merge)
     if w.prologue:
         pq, pk = ops.qk_norm_rope(dq, dk, *tabs, eps=w.eps)
