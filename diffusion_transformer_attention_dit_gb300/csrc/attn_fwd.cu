@@ -10,7 +10,9 @@
 //
 // Design (one CTA = 256 query rows of one (b, h), warp specialised):
 //   warp 8      TMA producer: Q tiles once, then K_j / V_j blocks of 128 keys
-//               into a ring of shared-memory slots (128-byte swizzle).
+//               into a ring of shared-memory slots (128-byte swizzle); a slot
+//               is refilled when the S-ready barrier of the second tile shows
+//               that its last reader has completed.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS form),
 //               O_t += P_t V_j with P read from TMEM (TS form).  Two query
 //               tiles t = 0, 1 alternate so the tensor core always has one
@@ -83,8 +85,8 @@ struct Layout {
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + kNQ * kTile;
   static constexpr int kBar = kKV + kSlots * kTile;
-  // q_full, slot_full[kSlots], slot_empty[kSlots], s_full[kNQ], p_full[kNQ], o_done[kNQ], drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 3 * kNQ + 1;
+  // q_full, slot_full[kSlots], s_full[kNQ], p_full[kNQ], o_done[kNQ], drain
+  static constexpr int kNumBars = 1 + kSlots + 3 * kNQ + 1;
   static constexpr int kTmemSlot = kBar + 8 * kNumBars;
   static constexpr int kBytes = kTmemSlot + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
@@ -149,18 +151,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = base + L::kBar;
   const uint32_t q_full = bars;
   auto slot_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto slot_empty = [&](int s) { return bars + 8u * (1 + kSlots + s); };
-  auto s_full = [&](int t) { return bars + 8u * (1 + 2 * kSlots + t); };
-  auto p_full = [&](int t) { return bars + 8u * (1 + 2 * kSlots + kNQ + t); };
-  auto o_done = [&](int t) { return bars + 8u * (1 + 2 * kSlots + 2 * kNQ + t); };
-  const uint32_t drain = bars + 8u * (1 + 2 * kSlots + 3 * kNQ);
+  auto s_full = [&](int t) { return bars + 8u * (1 + kSlots + t); };
+  auto p_full = [&](int t) { return bars + 8u * (1 + kSlots + kNQ + t); };
+  auto o_done = [&](int t) { return bars + 8u * (1 + kSlots + 2 * kNQ + t); };
+  const uint32_t drain = bars + 8u * (1 + kSlots + 3 * kNQ);
+  // K/V fill i (i < 2 * nblk) reuses the slot of fill i - kSlots, which may be
+  // overwritten once the last MMA reading it has completed.  K_b is read last by
+  // S_1(b), the last MMA issued for block b; V_b by P V_1(b), which S_1(b + 1)
+  // follows (for the last block, the o_done commits).  The s_full(1) / o_done(1)
+  // arrivals therefore also release the ring, and the MMA thread commits nothing
+  // for it.  The parity wait is exact because s_full(1) cannot run two phases
+  // ahead of a K/V fill: its next phase needs the fill being waited for.  Fills
+  // after the last K/V block (the update form's running O) wait for o_done(1)
+  // instead -- by then s_full(1) may have run ahead.
+  auto wait_slot_free = [&](int i) -> bool {
+    const int prev = i - kSlots;
+    if (prev < 0) return true;
+    const int blk = prev >> 1;
+    if ((prev & 1) == 0) return wait_bounded(s_full(kNQ - 1), blk & 1);
+    if (blk + 1 < nblk) return wait_bounded(s_full(kNQ - 1), (blk + 1) & 1);
+    return wait_bounded(o_done(kNQ - 1), 0);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(slot_full(s), 1);
-      mbar_init(slot_empty(s), 1);
-    }
+    for (int s = 0; s < kSlots; ++s) mbar_init(slot_full(s), 1);
     for (int t = 0; t < kNQ; ++t) {
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), 128);
@@ -197,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nblk && ok; ++j) {
         for (int which = 0; which < 2; ++which) {  // 0: K_j, 1: V_j
           const int i = 2 * j + which, slot = i % kSlots;
-          if (!wait_bounded(slot_empty(slot), ((i / kSlots) & 1) ^ 1)) {
+          if (!wait_slot_free(i)) {
             ok = false;
             break;
           }
@@ -214,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // half of an fp32 tile (boxes of 32 columns).
       for (int p = 0; p < acc_halves * kNQ && ok; ++p) {
         const int i = 2 * nblk + p, slot = i % kSlots, t = p % kNQ, hf = p / kNQ;
-        if (!wait_bounded(slot_empty(slot), ((i / kSlots) & 1) ^ 1)) {
+        if (!wait_bounded(o_done(kNQ - 1), 0)) {  // every MMA has completed: every slot is free
           ok = false;
           break;
         }
@@ -260,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(t, 0);
           tc_commit(s_full(t));
         }
-        tc_commit(slot_empty(0));
       }
       for (int j = 0; j < nblk && ok; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;
@@ -280,8 +294,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(slot_empty(iv % kSlots));
-        if (next) tc_commit(slot_empty(ik % kSlots));
       }
       if (ok)
         for (int t = 0; t < kNQ; ++t) tc_commit(o_done(t));
