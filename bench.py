@@ -62,7 +62,7 @@ MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", 
 PER_WORKLOAD = ("qwen_image", "qwen_image_edit", "wan480")
 # DRAM bytes (read + write) per attention launch, from an ncu capture of the attention source with this sha256
 # prefix; reported as roofline.traffic only while the source is unchanged.
-ATTN_TRAFFIC = {"source_sha256_prefix": "f32b5f4f04251cb4", "by_workload": {"wan720": 1717.2e6},
+ATTN_TRAFFIC = {"source_sha256_prefix": "fd1d8faa34948c3a", "by_workload": {"wan720": 1716.6e6},
                 "capture": "stored ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of one Wan2.2-720p "
                            "chunk launch, bench.py --profile-kernel attention --workload wan720"}
 
@@ -348,7 +348,7 @@ def made_events(n, stream):
     return evs
 
 
-def steps_for(dev_state, seconds: float, cap: int = 4000) -> int:
+def steps_for(dev_state, seconds: float, cap: int = 20000) -> int:
     """Steps that fill about `seconds` of timed work (one flushed step is measured first)."""
     import torch
 
@@ -397,7 +397,7 @@ def time_workload(ds, steps, uuid, world=1):
     res["wall_steps"] = wall1 - wall0
     # Attention region: dit_attention records its events on this stream right before the first and after the last
     # attention launch; one more event after the call closes the merge kernel.
-    attn_steps = min(steps, 1000)
+    attn_steps = steps
     n_ev = 3 if ds.merge_kernel else 2
     ev = made_events(n_ev * attn_steps, stream)
     with ClockSampler(uuid) as clocks:
