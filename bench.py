@@ -60,9 +60,9 @@ PARTIAL = {"tiny": "f32", "qwen_image": "f32", "qwen_image_edit": "f32", "wan480
 MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", "wan480": "kernel",
          "wan720": "kernel"}
 PER_WORKLOAD = ("qwen_image", "qwen_image_edit", "wan480")
-# DRAM bytes (read + write) per attention launch, from an ncu capture of the attention source with this sha256
-# prefix; reported as roofline.traffic only while the source is unchanged.
-ATTN_TRAFFIC = {"source_sha256_prefix": "fd1d8faa34948c3a", "by_workload": {"wan720": 1716.6e6},
+# DRAM bytes (read + write) per attention launch, from an ncu capture of the attention kernel whose code (source
+# without comments, attn_source_digest) has this sha256 prefix; reported as roofline.traffic only while it matches.
+ATTN_TRAFFIC = {"source_sha256_prefix": "ceeb94e64412b783", "by_workload": {"wan720": 1716.6e6},
                 "capture": "stored ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of one Wan2.2-720p "
                            "chunk launch, bench.py --profile-kernel attention --workload wan720"}
 
@@ -270,13 +270,22 @@ def config_of(w, chunks, args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def attn_traffic(name: str):
-    """ncu DRAM bytes per attention launch, or None if the kernel source changed since the capture."""
+def attn_source_digest() -> str:
+    """sha256 prefix of the attention kernel's source with comments and blank lines removed (comment edits keep
+    a stored capture valid; any code change invalidates it)."""
     import hashlib
+    import re
 
-    src = ROOT / "diffusion_transformer_attention_dit_gb300" / "csrc" / "attn_fwd.cu"
-    if ATTN_TRAFFIC["source_sha256_prefix"] is None or \
-            hashlib.sha256(src.read_bytes()).hexdigest()[:16] != ATTN_TRAFFIC["source_sha256_prefix"]:
+    text = (ROOT / "diffusion_transformer_attention_dit_gb300" / "csrc" / "attn_fwd.cu").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    code = "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
+
+
+def attn_traffic(name: str):
+    """ncu DRAM bytes per attention launch, or None if the kernel code changed since the capture."""
+    if ATTN_TRAFFIC["source_sha256_prefix"] != attn_source_digest():
         return None
     return ATTN_TRAFFIC["by_workload"].get(name)
 

@@ -160,10 +160,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // S_1(b), the last MMA issued for block b; V_b by P V_1(b), which S_1(b + 1)
   // follows (for the last block, the o_done commits).  The s_full(1) / o_done(1)
   // arrivals therefore also release the ring, and the MMA thread commits nothing
-  // for it.  The parity wait is exact because s_full(1) cannot run two phases
-  // ahead of a K/V fill: its next phase needs the fill being waited for.  Fills
-  // after the last K/V block (the update form's running O) wait for o_done(1)
-  // instead -- by then s_full(1) may have run ahead.
+  // for it.  A parity wait is exact while the barrier is at most one phase past
+  // the awaited one.  The producer waits for each s_full(1) phase (two fills per
+  // phase) as soon as it has issued the fill before, and the next phase needs a
+  // whole softmax pass of tile 1 after that one, so it sees every phase it waits
+  // for before the following one completes.  Were it ever two phases late, the
+  // wait would not return until a phase that needs this very fill: it times out
+  // and the launch reports an error; no slot is overwritten early.  Fills after
+  // the last K/V block (the update form's running O) wait for o_done(1) instead,
+  // which completes once.
   auto wait_slot_free = [&](int i) -> bool {
     const int prev = i - kSlots;
     if (prev < 0) return true;
