@@ -651,8 +651,9 @@ def run_ours(args):
 
 
 def run_ring_overlap(args):
-    """Diagnostic: the ring-overlap emulation (local attention || gather of the remote key shards, attention over
-    the gathered keys, merge) against the same steps run back to back on one stream."""
+    """Diagnostic: one rank's ring overlap (dit_attention_ring_overlap: local attention || device copies gathering
+    the remote key shards, then the attention over them merged in its epilogue) against the same work run back to
+    back on one stream."""
     import torch
 
     from diffusion_transformer_attention_dit_gb300 import build, ops
@@ -667,17 +668,28 @@ def run_ring_overlap(args):
     bounds = w.chunk_bounds(args.ring_overlap)
     k_loc, v_loc = k[:, :bounds[0][1]].contiguous(), v[:, :bounds[0][1]].contiguous()
     remote = [(k[:, lo:hi].contiguous(), v[:, lo:hi].contiguous()) for lo, hi in bounds[1:]]
-    side = torch.cuda.Stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    B, S, H, D = q.shape
+    s_rem = sum(b.shape[1] for b, _ in remote)
+    kr = torch.empty((B, s_rem, H, D), dtype=torch.bfloat16, device=dev)
+    vr = torch.empty_like(kr)
+    acc = torch.empty((B, S, H, D), dtype=torch.float32, device=dev)
+    o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    ws = torch.empty(ops.ring_overlap_workspace_bytes(B, S, H, D, s_rem, torch.float32), dtype=torch.uint8,
+                     device=dev)
 
-    def serial():
-        kr = torch.cat([a for a, _ in remote], dim=1)
-        vr = torch.cat([b for _, b in remote], dim=1)
-        o1, l1 = ops.attn_fwd(q, k_loc, v_loc, o_dtype=torch.float32)
-        return ops.attn_fwd_update(q, kr, vr, o1, l1, lse=l1)
+    def serial():  # the same work on one stream: gather copies, local attention, merged attention
+        off = 0
+        for kk, vv in remote:
+            kr[:, off:off + kk.shape[1]].copy_(kk)
+            vr[:, off:off + vv.shape[1]].copy_(vv)
+            off += kk.shape[1]
+        ops.attn_fwd(q, k_loc, v_loc, o=acc, lse=lse)
+        return ops.attn_fwd_update(q, kr, vr, acc, lse, o=o, lse=lse)
 
-    def overlapped():
-        return ops.ring_overlap_attention(q, k_loc, v_loc, remote, gather_stream=side)
+    def overlapped():  # dit_attention_ring_overlap: the gather on its own stream beside the local attention
+        return ops.ring_overlap_attention(q, k_loc, v_loc, remote, o=o, lse=lse, workspace=ws)
 
     res = {}
     for name, fn in (("serial", serial), ("overlapped", overlapped)):

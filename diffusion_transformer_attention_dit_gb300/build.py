@@ -20,7 +20,7 @@ INCLUDE = PKG.parent / "include"
 BUILD = PKG.parent / "_build"
 LIBRARY = PKG / "libditattn.so"
 SOURCES = ["api.cu", "attn_fwd.cu", "attn_merge.cu", "qk_norm_rope.cu", "row_kernels.cu", "fp8.cu", "host_path.cu",
-           "attention_path.cu", "attention_noalloc.cu"]
+           "attention_path.cu", "attention_noalloc.cu", "ring_overlap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

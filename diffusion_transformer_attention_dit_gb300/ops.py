@@ -22,7 +22,8 @@ EXPORTED = ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_merge_lse", "dit_poll_
             "dit_status_string", "dit_last_error_detail", "dit_selftest_wait_timeout", "dit_attn_fwd_causal",
             "dit_layer_norm_modulate", "dit_rms_norm", "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update",
             "dit_set_launch_overlap", "dit_attention_host", "dit_attention_host_workspace",
-            "dit_attention", "dit_attention_workspace", "dit_attention_noalloc", "dit_selftest_fp8_quotients")
+            "dit_attention", "dit_attention_workspace", "dit_attention_noalloc", "dit_selftest_fp8_quotients",
+            "dit_attention_ring_overlap", "dit_attention_ring_overlap_workspace")
 
 _lib = None
 
@@ -69,12 +70,18 @@ def load_library(path: Path | str = LIBRARY) -> ctypes.CDLL:
                                   i32, vp, vp, ctypes.c_size_t, vp, vp, vp]
     lib.dit_attention_workspace.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.dit_attention_workspace.restype = ctypes.c_size_t
+    lib.dit_attention_ring_overlap_workspace.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.dit_attention_ring_overlap_workspace.restype = ctypes.c_size_t
+    lib.dit_attention_ring_overlap.argtypes = [vp, vp, vp, i32, ctypes.POINTER(ctypes.c_void_p),
+                                               ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int), i32,
+                                               i32, i32, i32, i32, f32, i32, vp, i32, vp, vp, ctypes.c_size_t, vp]
     lib.dit_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, i32, i32,
                                           vp, i32, vp, vp]
     for name in ("dit_qk_norm_rope", "dit_attn_fwd", "dit_attn_fwd_causal", "dit_attn_merge_lse",
                  "dit_poll_device_error", "dit_selftest_wait_timeout", "dit_layer_norm_modulate", "dit_rms_norm",
                  "dit_quant_fp8_rows", "dit_gemm_fp8", "dit_attn_fwd_update", "dit_set_launch_overlap",
-                 "dit_attention_host", "dit_attention", "dit_attention_noalloc"):
+                 "dit_attention_host", "dit_attention", "dit_attention_noalloc", "dit_attention_ring_overlap",
+                 "dit_selftest_fp8_quotients"):
         getattr(lib, name).restype = ctypes.c_int
     lib.dit_status_string.argtypes = [ctypes.c_int]
     lib.dit_status_string.restype = ctypes.c_char_p
@@ -427,30 +434,45 @@ def dit_attention_host(q, k, v, wq=None, wk=None, cos=None, sin=None, eps: float
     return o, lse
 
 
-def ring_overlap_attention(q, k_local, v_local, remote_kv, scale: float | None = None, out_dtype=torch.bfloat16,
-                           partial_dtype=torch.float32, gather_stream=None):
-    """Two-attention ring overlap on one GPU ("NPU Wan2.2-I2V model inference optimisation
-    practice", section "Ring Attention Overlap").
+def ring_overlap_workspace_bytes(B, S, H, D, s_remote, partial_dtype=torch.float32) -> int:
+    """Device workspace bytes dit_attention_ring_overlap needs (s_remote = total remote keys)."""
+    return int(load_library().dit_attention_ring_overlap_workspace(B, S, H, D, s_remote, _dtype_code(partial_dtype)))
 
-    Attention over the local K/V runs on the current stream while the remote K/V
-    chunks are gathered into one contiguous buffer on `gather_stream` (device
-    copies stand in for the all-gather of a multi-GPU run); then one attention
-    over the gathered chunks whose epilogue LSE-merges it into the local result
-    (the update_out_and_lse step).  remote_kv is a list of (k_i, v_i) tensors
-    [B, S_i, H, D].  Returns (o, lse).
-    """
-    main = torch.cuda.current_stream()
-    side = gather_stream if gather_stream is not None else torch.cuda.Stream(device=q.device)
-    B, Sq, H, D = q.shape
-    side.wait_stream(main)  # the remote chunks must be ready before they are copied
-    with torch.cuda.stream(side):
-        k_r = torch.cat([kk for kk, _ in remote_kv], dim=1)
-        v_r = torch.cat([vv for _, vv in remote_kv], dim=1)
-        gathered = torch.cuda.Event()
-        gathered.record(side)
-    k_r.record_stream(main)
-    v_r.record_stream(main)
-    acc, lse = attn_fwd(q, k_local, v_local, scale, o_dtype=partial_dtype)
-    main.wait_event(gathered)
-    return attn_fwd_update(q, k_r, v_r, acc, lse, scale, o_dtype=out_dtype, lse=lse)
+
+def ring_overlap_attention(q, k_local, v_local, remote_kv, scale: float | None = None, out_dtype=torch.bfloat16,
+                           partial_dtype=torch.float32, o=None, lse=None, workspace=None, stream=None):
+    """One rank's ring-attention overlap on one GPU (dit_attention_ring_overlap; "NPU Wan2.2-I2V model inference
+    optimisation practice", section "Ring Attention Overlap").
+
+    The attention over the local K/V runs on the stream while the remote K/V shards are copied into one contiguous
+    buffer on a side stream (device copies stand in for the all-gather of a multi-GPU run); then one attention over
+    the gathered shards whose epilogue LSE-merges it into the local result (update_out_and_lse).  remote_kv is a
+    list of (k_i, v_i) contiguous bf16 tensors [B, S_i, H, D].  Returns (o, lse)."""
+    lib = load_library()
+    _cuda(q, k_local, v_local)
+    B, S, H, D = q.shape
+    s_local = k_local.shape[1]
+    for t in [q, k_local, v_local] + [x for kv in remote_kv for x in kv]:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v shards must be contiguous bf16 [B, S, H, D]")
+    if k_local.shape != v_local.shape or any(kk.shape != vv.shape for kk, vv in remote_kv):
+        raise ValueError("each shard's k and v must have the same shape")
+    R = len(remote_kv)
+    s_rem = [int(kk.shape[1]) for kk, _ in remote_kv]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if o is None:
+        o = torch.empty((B, S, H, D), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    wsb = ring_overlap_workspace_bytes(B, S, H, D, sum(s_rem), partial_dtype) if R else 0
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=q.device)
+    kp = (ctypes.c_void_p * max(R, 1))(*[kk.data_ptr() for kk, _ in remote_kv])
+    vp_ = (ctypes.c_void_p * max(R, 1))(*[vv.data_ptr() for _, vv in remote_kv])
+    sr = (ctypes.c_int * max(R, 1))(*s_rem)
+    _check(lib.dit_attention_ring_overlap(q.data_ptr(), k_local.data_ptr(), v_local.data_ptr(), s_local, kp, vp_, sr,
+                                          R, B, S, H, D, float(scale), _dtype_code(partial_dtype), o.data_ptr(),
+                                          _dtype_code(o.dtype), lse.data_ptr(), workspace.data_ptr(),
+                                          workspace.numel(), _stream(stream)))
+    return o, lse
 

@@ -15,6 +15,8 @@
  *   dit_attention       the whole hot path on device buffers, one call
  *   dit_attention_host  the whole hot path from host buffers, copies pipelined
  *                       against the kernels
+ *   dit_attention_ring_overlap  one rank's ring-attention overlap: local shard ||
+ *                       gather of the remote shards, then their LSE-merged attention
  *
  * Conventions shared by every entry point
  *   - Tensors are device pointers owned by the caller.  Activations are
@@ -389,6 +391,50 @@ dit_status dit_attention(const void *q, const void *k, const void *v,
                          dit_dtype partial_dtype, int merge_update, void *o, dit_dtype o_dtype, float *lse,
                          void *workspace, size_t workspace_bytes, struct CUevent_st *attn_begin,
                          struct CUevent_st *attn_end, struct CUstream_st *stream);
+
+/*
+ * dit_attention_ring_overlap -- the ring-attention overlap of one rank, on one GPU.
+ *
+ * Defined by: "NPU Wan2.2-I2V model inference optimisation practice", section
+ * "Ring Attention Overlap" (the attention over the local KV shard overlaps the
+ * gathering of the other ranks' shards; one more attention over the gathered
+ * keys, combined with the first by their LSEs), and "feat: support Ascend NPU
+ * backend (torch_npu) for Qwen-Image pipelines - #274", item 2
+ * (update_out_and_lse).
+ *
+ * Computes the attention of q over the keys local ++ remote_0 ++ ... ++
+ * remote_{R-1} (non-causal, as dit_attn_fwd over their concatenation) as:
+ *   - the R remote shards copied device-to-device into one contiguous
+ *     [B, sum(s_remote), H, D] buffer of the workspace, on a stream the call
+ *     creates (it waits for the caller's earlier work on `stream` first; on
+ *     one GPU these copies stand in for the all-gather);
+ *   - meanwhile, on `stream`, the attention over the local shard into a
+ *     running result (partial_dtype O in the workspace, LSE in `lse`);
+ *   - then, once the gather is done, the attention over the gathered keys
+ *     LSE-merged into that result in its epilogue (dit_attn_fwd_update's
+ *     kernel), writing o and lse.
+ * The call is complete on `stream` when it returns (the side stream is
+ * released by the runtime when its copies finish).  Results are bit-identical
+ * to dit_attn_fwd over the local shard followed by dit_attn_fwd_update over
+ * the concatenated remote shards.  R = 0 is plain attention over the local
+ * shard (no workspace needed).
+ *
+ *   q              bf16 [B, S, H, D], contiguous
+ *   k_local, v_local  bf16 [B, s_local, H, D], contiguous; s_local >= 1
+ *   k_remote, v_remote  HOST arrays of R device pointers; shard r is bf16
+ *                  [B, s_remote[r], H, D], contiguous, 16-byte aligned; s_remote[r] >= 1
+ *   partial_dtype  dtype of the local running O in the workspace (DIT_F32 recommended)
+ *   o, lse         outputs as for dit_attn_fwd (contiguous), not overlapping any input
+ *   workspace      >= dit_attention_ring_overlap_workspace(B, S, H, D, sum(s_remote),
+ *                  partial_dtype) bytes, 256-byte aligned, not overlapping any argument
+ * Argument errors return before anything is queued.
+ */
+size_t dit_attention_ring_overlap_workspace(int B, int S, int H, int D, int s_remote, dit_dtype partial_dtype);
+dit_status dit_attention_ring_overlap(const void *q, const void *k_local, const void *v_local, int s_local,
+                                      const void *const *k_remote, const void *const *v_remote,
+                                      const int *s_remote, int R, int B, int S, int H, int D, float scale,
+                                      dit_dtype partial_dtype, void *o, dit_dtype o_dtype, float *lse,
+                                      void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
  * dit_attention_noalloc -- dit_attention for callers that cannot allocate

@@ -120,6 +120,47 @@ def test_update_empty_work_is_ok_without_launch(lib):
     assert _update(lib, B=0, acc=None) == ops.DIT_OK
 
 
+def _ring(lib, **kw):
+    a = dict(q=A16, kl=A16 * 2, vl=A16 * 3, sl=256, kr=[A16 * 4], vr=[A16 * 5], sr=[256], B=1, S=256, H=2, D=128,
+             scale=0.088, pdt=1, o=A16 * 8, odt=0, lse=A16 * 16, ws=A16 * 64, wsb=1 << 30)
+    a.update(kw)
+    R = len(a["kr"])
+    kr = (ctypes.c_void_p * max(R, 1))(*a["kr"])
+    vr = (ctypes.c_void_p * max(R, 1))(*a["vr"])
+    sr = (ctypes.c_int * max(len(a["sr"]), 1))(*a["sr"])
+    return lib.dit_attention_ring_overlap(a["q"], a["kl"], a["vl"], a["sl"], kr, vr, sr, a.get("R", R), a["B"],
+                                          a["S"], a["H"], a["D"], a["scale"], a["pdt"], a["o"], a["odt"], a["lse"],
+                                          a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(R=-1), ops.DIT_ERR_INVALID_ARG),
+    (dict(sl=0), ops.DIT_ERR_INVALID_ARG),
+    (dict(sr=[0]), ops.DIT_ERR_INVALID_ARG),              # an empty remote shard
+    (dict(kr=[None]), ops.DIT_ERR_INVALID_ARG),
+    (dict(vr=[A16 * 5 + 8]), ops.DIT_ERR_INVALID_ARG),    # remote shard misaligned
+    (dict(D=80), ops.DIT_ERR_UNSUPPORTED),
+    (dict(pdt=4), ops.DIT_ERR_INVALID_ARG),
+    (dict(q=A16 + 4), ops.DIT_ERR_INVALID_ARG),
+    (dict(scale=0.0), ops.DIT_ERR_INVALID_ARG),
+    (dict(o=A16 * 4), ops.DIT_ERR_INVALID_ARG),           # output over a remote shard
+    (dict(lse=A16 * 8 + 64), ops.DIT_ERR_INVALID_ARG),    # lse inside o
+    (dict(ws=None), ops.DIT_ERR_INVALID_ARG),
+    (dict(ws=A16 * 64 + 16), ops.DIT_ERR_INVALID_ARG),    # workspace misaligned
+    (dict(wsb=1024), ops.DIT_ERR_INVALID_ARG),            # workspace too small
+    (dict(ws=A16 * 8), ops.DIT_ERR_INVALID_ARG),          # workspace over o
+])
+def test_ring_overlap_rejects_bad_arguments(lib, kw, code):
+    assert _ring(lib, **kw) == code
+    assert lib.dit_last_error_detail() != b""
+
+
+def test_ring_overlap_workspace_and_empty_work(lib):
+    assert lib.dit_attention_ring_overlap_workspace(1, 256, 2, 128, 256, 1) >= 2 * 256 * 2 * 128 * 2 + 256 * 2 * 128 * 4
+    assert lib.dit_attention_ring_overlap_workspace(1, 256, 2, 128, -1, 1) == 0
+    assert _ring(lib, B=0) == ops.DIT_OK
+
+
 def _prologue(lib, **kw):
     a = dict(q=A16, k=A16 * 2, qo=A16 * 3, ko=A16 * 4, wq=A16 * 5, wk=A16 * 6, cos=A16 * 7, sin=A16 * 8, B=1, S=16,
              H=2, D=128, eps=1e-6)

@@ -439,6 +439,37 @@ def test_ring_overlap_equals_full_attention(orc):
     check_lse(host_f64(lse), rl, what="ring overlap")
 
 
+@pytest.mark.parametrize("B,H,D,local,remote_lens,pdt", [
+    (2, 3, 128, 300, [129, 1, 400], "f32"),   # batch of 2 (strided gather), ragged shards, a one-key shard
+    (1, 2, 64, 64, [64, 64, 64, 64, 64, 64, 64], "bf16"),
+    (1, 4, 128, 517, [], "f32"),              # a ring of one rank: plain attention
+])
+def test_ring_overlap_equals_its_entry_points(orc, B, H, D, local, remote_lens, pdt):
+    """dit_attention_ring_overlap == dit_attn_fwd over the local shard then dit_attn_fwd_update over the
+    concatenated remote shards, bit for bit; and == the oracle's attention over all keys."""
+    dts = {"bf16": torch.bfloat16, "f32": torch.float32}
+    S = local + sum(remote_lens)
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=S + B, k_std=2.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    edges = [local]
+    for n in remote_lens:
+        edges.append(edges[-1] + n)
+    remote = [(tk[:, a:b].contiguous(), tv[:, a:b].contiguous()) for a, b in zip(edges[:-1], edges[1:])]
+    kl, vl = tk[:, :local].contiguous(), tv[:, :local].contiguous()
+    o, lse = ops.ring_overlap_attention(tq, kl, vl, remote, partial_dtype=dts[pdt])
+    if remote_lens:
+        acc, rl = ops.attn_fwd(tq, kl, vl, o_dtype=dts[pdt])
+        ro, rl = ops.attn_fwd_update(tq, tk[:, local:].contiguous(), tv[:, local:].contiguous(), acc, rl, lse=rl)
+    else:
+        ro, rl = ops.attn_fwd(tq, kl, vl)
+    torch.cuda.synchronize()
+    ops.poll_device_error()
+    assert torch.equal(o, ro) and torch.equal(lse, rl)
+    fo, fl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
+    check_o(host_f64(o), fo, what="ring overlap", vmax=vmax(v))
+    check_lse(host_f64(lse), fl, what="ring overlap")
+
+
 # ---------------------------------------------------------------- W8A8 fp8
 
 @pytest.mark.parametrize("M,K", [(7, 3072), (300, 128), (1, 16), (64, 8192)])
