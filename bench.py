@@ -62,7 +62,7 @@ MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", 
 PER_WORKLOAD = ("qwen_image", "qwen_image_edit", "wan480")
 # DRAM bytes (read + write) per attention launch, from an ncu capture of the attention kernel whose code (source
 # without comments, attn_source_digest) has this sha256 prefix; reported as roofline.traffic only while it matches.
-ATTN_TRAFFIC = {"source_sha256_prefix": "ceeb94e64412b783", "by_workload": {"wan720": 1716.6e6},
+ATTN_TRAFFIC = {"source_sha256_prefix": "54550daf04c30c11", "by_workload": {"wan720": 1716.6e6},
                 "capture": "stored ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of one Wan2.2-720p "
                            "chunk launch, bench.py --profile-kernel attention --workload wan720"}
 
@@ -501,7 +501,7 @@ def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
     for _ in range(max(1, warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    t = 0.0
+    ts = []
     for _ in range(steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -509,10 +509,10 @@ def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
         e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        t += e0.elapsed_time(e1) / 1e3
+        ts.append(e0.elapsed_time(e1) / 1e3)
     ops.poll_device_error()
     del ws
-    return t, h2d, d2h
+    return ts, h2d, d2h
 
 
 def per_workload_record(name, args, dev, uuid, pk, src):
@@ -598,10 +598,14 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
-        t_e2e, h2d, d2h = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
+        ts_e2e, h2d, d2h = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
+        t_e2e = sum(ts_e2e)
         _, e2e_value = aggregate(t_e2e, flops_step, e2e_steps, world, dev)
         e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps, "ms_per_step": t_e2e / e2e_steps * 1e3,
+               # the spread of the steps (the host link is shared with the machine's other GPUs)
+               "ms_per_step_min": min(ts_e2e) * 1e3, "ms_per_step_median": statistics.median(ts_e2e) * 1e3,
+               "ms_per_step_max": max(ts_e2e) * 1e3,
                "api": "dit_attention_host (" + ("query ranges, stacked partials + merge kernel per range, each "
                                                 "range's O copied back while the next computes" if
                                                 (merge == "kernel" or chunks == 1) else

@@ -122,6 +122,23 @@ def test_attn_fwd_sharp_softmax_rescale(orc):
     check_lse(host_f64(lse), rl, what="sharp")
 
 
+def test_attn_fwd_rescale_with_growing_scores(orc):
+    """Keys whose scores rise by about 20 (base-2 units) from one 128-key block to the next: every row's running
+    max is raised, and O rescaled, on every block."""
+    B, H, S, D = 1, 2, 640, 128
+    rng = np.random.default_rng(12)
+    q = np.ones((B, S, H, D), np.float32) + 0.05 * rng.standard_normal((B, S, H, D)).astype(np.float32)
+    ramp = (np.arange(S) // 128).astype(np.float32)[None, :, None, None] * 1.25
+    k = ramp * np.ones((B, S, H, D), np.float32) + 0.05 * rng.standard_normal((B, S, H, D)).astype(np.float32)
+    v = rng.standard_normal((B, S, H, D)).astype(np.float32)
+    qb, kb, vb = (inputs.f32_to_bf16_bits(x) for x in (q, k, v))
+    scale = 1 / math.sqrt(D)
+    o, lse = ops.attn_fwd(dev_bf16(qb), dev_bf16(kb), dev_bf16(vb), scale, o_dtype=torch.float32)
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (qb, kb, vb)), scale)
+    check_o(host_f64(o), ro, f32=True, what="growing scores", vmax=vmax(vb))
+    check_lse(host_f64(lse), rl, what="growing scores")
+
+
 # ---------------------------------------------------------------- merge
 
 @pytest.mark.parametrize("C", [1, 2, 3, 8, 20])  # 20 parts take the register (non-bulk) path
