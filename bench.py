@@ -493,6 +493,16 @@ def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
                      dtype=torch.uint8, device=dev)
     tabs = small if w.prologue else [None] * 4
     stream = torch.cuda.current_stream()
+    # the host link's rate right now (it is shared with the machine's other GPUs): one pinned copy of q
+    probe = torch.empty(pin["q"].numel(), dtype=torch.int16, device=dev)
+    probe.copy_(pin["q"], non_blocking=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    probe.copy_(pin["q"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_gbps = probe.numel() * 2 / e0.elapsed_time(e1) / 1e6
+    del probe
 
     def e2e_step():
         ops.dit_attention_host(hq, hk, hv, *tabs, eps=w.eps, chunks=chunks, partial_dtype=pdt, prologue=w.prologue,
@@ -512,7 +522,7 @@ def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
         ts.append(e0.elapsed_time(e1) / 1e3)
     ops.poll_device_error()
     del ws
-    return ts, h2d, d2h
+    return ts, h2d, d2h, h2d_gbps
 
 
 def per_workload_record(name, args, dev, uuid, pk, src):
@@ -598,7 +608,7 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
-        ts_e2e, h2d, d2h = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
+        ts_e2e, h2d, d2h, h2d_gbps = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
         t_e2e = sum(ts_e2e)
         _, e2e_value = aggregate(t_e2e, flops_step, e2e_steps, world, dev)
         e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -606,6 +616,7 @@ def run_ours(args):
                # the spread of the steps (the host link is shared with the machine's other GPUs)
                "ms_per_step_min": min(ts_e2e) * 1e3, "ms_per_step_median": statistics.median(ts_e2e) * 1e3,
                "ms_per_step_max": max(ts_e2e) * 1e3,
+               "host_to_device_GBps": h2d_gbps,
                "api": "dit_attention_host (" + ("query ranges, stacked partials + merge kernel per range, each "
                                                 "range's O copied back while the next computes" if
                                                 (merge == "kernel" or chunks == 1) else

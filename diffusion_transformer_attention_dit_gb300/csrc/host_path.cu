@@ -13,9 +13,10 @@
 // at the end.
 //
 // Query-range form (merge_update = 0, or a single chunk): the query rows are
-// processed in R ranges whose edges are multiples of 256 rows (one attention
-// CTA's rows), so each range runs exactly the tiles the one-call device path
-// runs and gives bit-identical results.  For range r: every KV chunk's
+// processed in R ranges (large problems: six, of 3/8 down to 1/16 of the rows)
+// whose edges are multiples of 256 rows (one attention CTA's rows), so each
+// range runs exactly the tiles the one-call device path runs and gives
+// bit-identical results.  For range r: every KV chunk's
 // attention over the range's rows into stacked partials, the merge kernel into
 // one of two output staging buffers, and -- on the output-copy stream -- the
 // copy of that range's O and LSE to the host, which overlaps the next range's
@@ -45,24 +46,38 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool range_form(int chunks, int merge_update) { return chunks == 1 || merge_update == 0; }
 
-// Number of query ranges: as many as keep every range's launches at least
-// kMinRangeCtas CTAs, at most kMaxRanges.
+// Tapered ranges, for problems large enough that a sixteenth of the rows still
+// makes kMinRangeCtas CTAs: six ranges ending at 6, 10, 12, 14, 15 and 16
+// sixteenths of the rows.  The first range's attention (3/8 of the work) then
+// outlasts the copy of every chunk's keys and values even over a host link
+// shared with other work (it needs all of them), and the last range, whose
+// output copy is the one left exposed, is 1/16 of the rows.
+constexpr int kTaperRanges = 6;
+constexpr int kTaperEnd[kTaperRanges] = {6, 10, 12, 14, 15, 16};
+
+bool tapered(int B, int S, int H) { return (int64_t)B * H * (S / 16 / kRangeRows) >= kMinRangeCtas; }
+
+// Number of query ranges: the tapered six, or as many equal ranges as keep every
+// range's launches at least kMinRangeCtas CTAs, at most kMaxRanges.
 int query_ranges(int B, int S, int H) {
+  if (tapered(B, S, H)) return kTaperRanges;
   const int64_t bh = std::max<int64_t>(1, (int64_t)B * H);
   const int64_t rows_min = (kMinRangeCtas + bh - 1) / bh * kRangeRows;
   return (int)std::max<int64_t>(1, std::min<int64_t>(kMaxRanges, S / rows_min));
 }
 
-// First row of range r of R over S rows (edges rounded down to kRangeRows).
-int range_edge(int r, int R, int S) {
+// First row of range r of the R = query_ranges(B, S, H) ranges over S rows
+// (edges rounded down to kRangeRows).
+int range_edge(int r, int R, int B, int S, int H) {
   if (r <= 0) return 0;
   if (r >= R) return S;
+  if (tapered(B, S, H)) return (int)((int64_t)S * kTaperEnd[r - 1] / 16 / kRangeRows * kRangeRows);
   return (int)((int64_t)r * S / R / kRangeRows * kRangeRows);
 }
 
-int max_range_rows(int R, int S) {
+int max_range_rows(int R, int B, int S, int H) {
   int m = 0;
-  for (int r = 0; r < R; ++r) m = std::max(m, range_edge(r + 1, R, S) - range_edge(r, R, S));
+  for (int r = 0; r < R; ++r) m = std::max(m, range_edge(r + 1, R, B, S, H) - range_edge(r, R, B, S, H));
   return m;
 }
 
@@ -96,7 +111,7 @@ WsLayout plan(int B, int S, int H, int D, int chunks, int prologue, dit_dtype pa
   }
   if (range_form(chunks, merge_update)) {
     L.ranges = query_ranges(B, S, H);
-    L.range_rows = max_range_rows(L.ranges, S);
+    L.range_rows = max_range_rows(L.ranges, B, S, H);
     const size_t relems = (size_t)B * L.range_rows * H * D, rlse = (size_t)B * H * L.range_rows * 4;
     if (chunks > 1) {
       L.parts = take(relems * psize * chunks);
@@ -217,7 +232,7 @@ dit_status dit_attention_host(const void *q, const void *k, const void *v, const
           ok(cudaMemcpyAsync(ws + L.sn, sin_tab, tab, cudaMemcpyHostToDevice, cin));
     }
   } else {
-    ok(copy_rows_in(ws + L.q, q, B, S, row, 0, range_edge(1, R, S), cin)) && ok(cudaEventRecord(ev_q[0], cin));
+    ok(copy_rows_in(ws + L.q, q, B, S, row, 0, range_edge(1, R, B, S, H), cin)) && ok(cudaEventRecord(ev_q[0], cin));
   }
   ok(cudaEventRecord(ev[1], cin));
   for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
@@ -226,7 +241,7 @@ dit_status dit_attention_host(const void *q, const void *k, const void *v, const
     ok(copy_rows_in(ws + L.v, v, B, S, row, lo, hi, cin)) && ok(cudaEventRecord(ev[2 + c], cin));
   }
   for (int r = 1; r < R && !prologue && e == cudaSuccess; ++r)
-    ok(copy_rows_in(ws + L.q, q, B, S, row, range_edge(r, R, S), range_edge(r + 1, R, S), cin)) &&
+    ok(copy_rows_in(ws + L.q, q, B, S, row, range_edge(r, R, B, S, H), range_edge(r + 1, R, B, S, H), cin)) &&
         ok(cudaEventRecord(ev_q[r], cin));
   if (e != cudaSuccess) return host_fail(DIT_ERR_CUDA, cudaGetErrorString(e));
 
@@ -266,7 +281,7 @@ dit_status dit_attention_host(const void *q, const void *k, const void *v, const
   const size_t psize = partial_dtype == DIT_F32 ? 4 : 2, osize = o_dtype == DIT_F32 ? 4 : 2;
   const int64_t kv_st[3] = {(int64_t)S * H * D, (int64_t)H * D, D};
   for (int r = 0; r < R; ++r) {
-    const int r0 = range_edge(r, R, S), rows = range_edge(r + 1, R, S) - r0;
+    const int r0 = range_edge(r, R, B, S, H), rows = range_edge(r + 1, R, B, S, H) - r0;
     const int64_t part_o = (int64_t)B * rows * H * D, part_l = (int64_t)B * H * rows;
     const int64_t o_st[3] = {(int64_t)rows * H * D, (int64_t)H * D, D};
     const char *qr = static_cast<const char *>(dq) + (size_t)r0 * row;

@@ -301,7 +301,11 @@ dit_status dit_gemm_fp8(const void *a, const float *a_scale, const void *b, cons
  *     back at the end.
  *   merge_update = 0, or chunks == 1: the query rows are processed in up to 8
  *     ranges whose edges are multiples of 256 rows (fewer ranges when a range
- *     would hold fewer than 608 query tiles of 256 rows over all (b, h)).  Per
+ *     would hold fewer than 608 query tiles of 256 rows over all (b, h)); when
+ *     even a sixteenth of the rows makes 608 tiles, six ranges of 3/8, 1/4,
+ *     1/8, 1/8, 1/16 and 1/16 of the rows (the first range's attention then
+ *     covers the copy of every chunk's keys and values, the last range's
+ *     output copy is short).  Per
  *     range: dit_attn_fwd over every chunk into stacked partials of
  *     partial_dtype, dit_attn_merge_lse (chunks > 1), and the range's O and
  *     LSE copied back while the next range computes.  Without the prologue the

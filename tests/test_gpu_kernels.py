@@ -608,6 +608,7 @@ def test_w8a8_projection_accuracy():
     (1, 6000, 64, 64, 3, False, "bf16", "bf16", True, "kernel"),  # two query ranges (a ragged one)
     (4, 2100, 152, 64, 3, True, "f32", "bf16", True, "kernel"),   # eight query ranges, B = 4, prologue
     (1, 8000, 64, 128, 1, False, "bf16", "f32", True, "kernel"),  # one chunk over three query ranges
+    (1, 16384, 152, 64, 2, False, "bf16", "bf16", True, "kernel"),  # six tapered query ranges (3/8 ... 1/16)
     (2, 1000, 3, 128, 2, False, "f32", "bf16", False, "kernel"),  # pageable host memory
 ])
 def test_attention_host_matches_device_path(orc, B, S, H, D, chunks, prologue, pdt, odt, pinned, merge):
