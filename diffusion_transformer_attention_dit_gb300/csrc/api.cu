@@ -332,7 +332,8 @@ dit_status dit_selftest_fp8_quotients(uint64_t counts[2], struct CUstream_st *st
   g_detail = "";
   if (!counts) return fail(DIT_ERR_INVALID_ARG, "null counts");
   unsigned long long c[2] = {0ull, 0ull};
-  const dit_status st = from_cuda(ditattn::run_fp8_quotient_selftest(c, reinterpret_cast<cudaStream_t>(stream)), nullptr);
+  const cudaError_t e = ditattn::run_fp8_quotient_selftest(c, reinterpret_cast<cudaStream_t>(stream));
+  const dit_status st = from_cuda(e, nullptr);
   counts[0] = c[0];
   counts[1] = c[1];
   return st;

@@ -14,6 +14,7 @@
 // reaches memory, only the merged O and LSE.
 
 #include <cuda_runtime.h>
+#include <math.h>
 
 #include "../../include/ditattn.h"
 #include "internal.h"
@@ -98,7 +99,7 @@ dit_status dit_attention_ring_overlap(const void *q, const void *k_local, const 
   }
   if (s_rt > (int64_t)1 << 30) return ring_fail(DIT_ERR_INVALID_ARG, "remote shards too long");
   if ((int64_t)B * S * H == 0) return DIT_OK;
-  if (!(scale > 0.f) || scale > 3.0e38f) return ring_fail(DIT_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (!(scale > 0.f) || isinf(scale)) return ring_fail(DIT_ERR_INVALID_ARG, "scale must be finite and > 0");
   // the checks the attention launches would make, before any copy is queued
   if (!q || !k_local || !v_local || !o || !lse) return ring_fail(DIT_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(q) || !aligned16(k_local) || !aligned16(v_local) || !aligned16(o) ||
@@ -115,9 +116,11 @@ dit_status dit_attention_ring_overlap(const void *q, const void *k_local, const 
     if ((o0 < l1 && l0 < o1) || hits(q, act * 2) || hits(k_local, (size_t)B * s_local * H * D * 2) ||
         hits(v_local, (size_t)B * s_local * H * D * 2))
       return ring_fail(DIT_ERR_INVALID_ARG, "outputs overlap inputs or each other");
-    for (int r = 0; r < R; ++r)
-      if (hits(k_remote[r], (size_t)B * s_remote[r] * H * D * 2) || hits(v_remote[r], (size_t)B * s_remote[r] * H * D * 2))
+    for (int r = 0; r < R; ++r) {
+      const size_t shard = (size_t)B * s_remote[r] * H * D * 2;
+      if (hits(k_remote[r], shard) || hits(v_remote[r], shard))
         return ring_fail(DIT_ERR_INVALID_ARG, "outputs overlap a remote shard");
+    }
   }
   const RingWs L = ring_plan(B, S, H, D, (int)s_rt, partial_dtype);
   if (R > 0) {
