@@ -192,6 +192,46 @@ def test_chunked_merged_equals_full(orc, C, partial):
         assert (host_f64(om) - host_f64(o_parts[c])).__abs__().max() > 0.05
 
 
+@pytest.mark.parametrize("edges,partial", [
+    ([0, 1, 64, 65, 300, 500], "f32"),              # unequal chunks, two of one key
+    ([0, 1, 64, 65, 300, 500], "bf16"),
+    ([0, 500], "f32"),                              # C = 1: the merge of one part is that part
+    ([0, 63, 127, 128, 250, 251, 380, 499, 500], "f32"),  # C = 8, ragged against the 128-key blocks
+])
+def test_merged_unequal_chunks_equal_single_pass(orc, edges, partial):
+    """Unequal key chunks (including chunks of one key, C = 1 and C = 8) merged by LSE: every element against the
+    single pass on the GPU and against the oracle."""
+    B, H, S, D = 2, 3, 500, 128
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=len(edges) * 13, k_std=2.0)
+    tq, tk, tv = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    dt = torch.float32 if partial == "f32" else torch.bfloat16
+    C = len(edges) - 1
+    o_parts = torch.empty((C, B, S, H, D), dtype=dt, device="cuda")
+    lse_parts = torch.empty((C, B, H, S), dtype=torch.float32, device="cuda")
+    for c in range(C):
+        ops.attn_fwd(tq, tk, tv, None, edges[c], edges[c + 1], o=o_parts[c], lse=lse_parts[c])
+    om, lm = ops.attn_merge_lse(o_parts, lse_parts, out_dtype=torch.bfloat16)
+    of, lf = ops.attn_fwd(tq, tk, tv)
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
+    check_o(host_f64(om), ro, what=f"merged {edges} vs oracle")
+    check_lse(host_f64(lm), rl, what=f"merged {edges} vs oracle")
+    check_o(host_f64(om), host_f64(of), what=f"merged {edges} vs single pass")
+    check_lse(host_f64(lm), host_f64(lf), what=f"merged {edges} vs single pass")
+
+
+@pytest.mark.parametrize("S", [1, 63, 64, 127, 129, 200, 4312])
+@pytest.mark.parametrize("D", [64, 128])
+def test_attn_fwd_tail_lengths(orc, S, D):
+    """Sequence lengths around the 128-row tiles and 128-key blocks (and the Qwen-Image length), every element
+    against the oracle."""
+    B, H = 1, 2
+    q, k, v, *_ = inputs.small_case(B, S, H, D, seed=S * 3 + D)
+    o, lse = ops.attn_fwd(dev_bf16(q), dev_bf16(k), dev_bf16(v))
+    ro, rl = orc.attention(*(inputs.bf16_bits_to_f64(x) for x in (q, k, v)), 1 / math.sqrt(D))
+    check_o(host_f64(o), ro, what=f"S {S} D {D}")
+    check_lse(host_f64(lse), rl, what=f"S {S} D {D}")
+
+
 def test_fp32_partials_merge_closer_to_the_oracle_than_bf16(orc):
     """Ring attention that merges bf16-rounded block outputs loses accuracy (the reason this library offers fp32
     partials).  On the Wan2.2-720p-style sharp softmax (K drawn x 3, 8 KV chunks, stacked partials + merge kernel,

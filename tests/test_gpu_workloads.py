@@ -84,3 +84,23 @@ def test_workload_parity(name, chunks, merge):
         ref_l[:, h:h + 1, :] = lh
     check_o(got_o, ref_o, what=f"{name} merged vs oracle (sampled rows)")
     check_lse(got_l, ref_l, what=f"{name} merged vs oracle (sampled rows)")
+
+
+def test_qwen_image_every_element():
+    """Qwen-Image (B1 H24 S4312, prologue, one pass, as bench.py runs it): every element of O and LSE against the
+    oracle (its prologue in fp64, rounded to bf16 as the kernel hands Q and K to the attention)."""
+    orc = oracle.get()
+    inp = inputs.make_inputs("qwen_image")
+    w = inp.w
+    dq, dk, dv = dev_bf16(inp.q), dev_bf16(inp.k), dev_bf16(inp.v)
+    tabs = (dev_f32(inp.wq), dev_f32(inp.wk), dev_f32(inp.cos), dev_f32(inp.sin))
+    o, lse = ops.dit_attention(dq, dk, dv, *tabs, eps=w.eps, chunks=1, prologue=True)
+    ops.poll_device_error()
+    c64, s64 = inp.cos.astype(np.float64), inp.sin.astype(np.float64)
+    q = oracle.round_bf16(orc.qk_norm_rope(inputs.bf16_bits_to_f64(inp.q), inp.wq.astype(np.float64), c64, s64,
+                                           w.eps))
+    k = oracle.round_bf16(orc.qk_norm_rope(inputs.bf16_bits_to_f64(inp.k), inp.wk.astype(np.float64), c64, s64,
+                                           w.eps))
+    ro, rl = orc.attention(q, k, inputs.bf16_bits_to_f64(inp.v), w.scale)
+    check_o(host_f64(o), ro, what="qwen_image every element")
+    check_lse(host_f64(lse), rl, what="qwen_image every element")
