@@ -494,7 +494,7 @@ def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
     tabs = small if w.prologue else [None] * 4
     stream = torch.cuda.current_stream()
     # the host link's rate right now (it is shared with the machine's other GPUs): one pinned copy of q
-    probe = torch.empty(pin["q"].numel(), dtype=torch.int16, device=dev)
+    probe = torch.empty_like(pin["q"], device=dev)
     probe.copy_(pin["q"], non_blocking=True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
