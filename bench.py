@@ -511,18 +511,20 @@ def e2e_measure(inp, chunks, merge, steps, warmup, dev, flush):
     for _ in range(max(1, warmup)):
         e2e_step()
     torch.cuda.synchronize()
-    ts = []
+    ts, host = [], []
     for _ in range(steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        t0 = time.perf_counter()
         e2e_step()
+        host.append(time.perf_counter() - t0)  # how long the call took to queue the step's work
         e1.record(stream)
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1) / 1e3)
     ops.poll_device_error()
     del ws
-    return ts, h2d, d2h, h2d_gbps
+    return ts, h2d, d2h, h2d_gbps, host
 
 
 def per_workload_record(name, args, dev, uuid, pk, src):
@@ -608,7 +610,7 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
-        ts_e2e, h2d, d2h, h2d_gbps = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
+        ts_e2e, h2d, d2h, h2d_gbps, host = e2e_measure(inp, chunks, merge, e2e_steps, args.warmup, dev, ds.flush)
         t_e2e = sum(ts_e2e)
         _, e2e_value = aggregate(t_e2e, flops_step, e2e_steps, world, dev)
         e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -617,6 +619,7 @@ def run_ours(args):
                "ms_per_step_min": min(ts_e2e) * 1e3, "ms_per_step_median": statistics.median(ts_e2e) * 1e3,
                "ms_per_step_max": max(ts_e2e) * 1e3,
                "host_to_device_GBps": h2d_gbps,
+               "host_call_ms_median": statistics.median(host) * 1e3, "host_call_ms_max": max(host) * 1e3,
                "api": "dit_attention_host (" + ("query ranges, stacked partials + merge kernel per range, each "
                                                 "range's O copied back while the next computes" if
                                                 (merge == "kernel" or chunks == 1) else
