@@ -301,12 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (next) {
             issue_s(t, ik % kSlots);
             tc_commit(s_full(t));
+          } else {
+            // tile t's O is final once this P V is: its epilogue need not wait for the other tile's
+            tc_commit(o_done(t));
           }
         }
         if (!ok) break;
       }
-      if (ok)
-        for (int t = 0; t < kNQ; ++t) tc_commit(o_done(t));
       // Every MMA issued must complete before TMEM is freed.
       tc_commit(drain);
       wait_bounded(drain, 0);
