@@ -454,7 +454,12 @@ def test_attn_fwd_causal_chunks_merge(orc):
 
 # ---------------------------------------------------------------- LayerNorm-modulate / RMSNorm over C
 
-@pytest.mark.parametrize("B,L,C", [(2, 37, 3072), (1, 130, 5120), (3, 5, 8), (1, 7, 8192), (2, 300, 128)])
+# odd L: a row pair of the two-row kernel straddles two batch entries; an odd row
+# count leaves a last pair of one row; (3, 1001, 1024) and (2, 2049, 5120) give
+# every CTA several pairs; C = 7168 is the widest row of the two-row kernel,
+# C = 8192 the one-row kernel's
+@pytest.mark.parametrize("B,L,C", [(2, 37, 3072), (1, 130, 5120), (3, 5, 8), (1, 7, 8192), (2, 300, 128),
+                                   (3, 3, 7168), (3, 1001, 1024), (2, 2049, 5120)])
 def test_layer_norm_modulate_parity(orc, B, L, C):
     rng = np.random.default_rng(C + L)
     x = inputs.bf16_normal(B * L * C, seed=C + 7, std=2.0, mean=0.3).reshape(B, L, C)
