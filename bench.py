@@ -894,24 +894,45 @@ def run_qkv_fp8(args):
     xs = torch.empty(M, dtype=torch.float32, device=dev)
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    tq, tg = [], []
-    for i in range(args.warmup + max(args.steps, 5)):
-        flush.zero_()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record()
-        ops.quant_fp8_rows(x, xq, xs)
-        e[1].record()
-        ops.gemm_fp8(xq, xs, wq, ws, out=out)
-        e[2].record()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001
+        pass
+    # a region of about REGION_S seconds, so the clock record holds samples under load
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    ops.quant_fp8_rows(x, xq, xs)
+    ops.gemm_fp8(xq, xs, wq, ws, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    steps = int(min(20000, max(args.steps, 20, REGION_S * 1e3 / (e0.elapsed_time(e1) + 0.05))))
+    ev = made_events(3 * (args.warmup + steps), torch.cuda.current_stream())
+    with ClockSampler(uuid) as clocks:
+        clocks.ready()
         torch.cuda.synchronize()
-        if i >= args.warmup:
-            tq.append(e[0].elapsed_time(e[1]))
-            tg.append(e[1].elapsed_time(e[2]))
+        wall0 = time.perf_counter()
+        for i in range(args.warmup + steps):
+            flush.zero_()
+            ev[3 * i].record()
+            ops.quant_fp8_rows(x, xq, xs)
+            ev[3 * i + 1].record()
+            ops.gemm_fp8(xq, xs, wq, ws, out=out)
+            ev[3 * i + 2].record()
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
     ops.poll_device_error()
-    t_q, t_g = statistics.median(tq), statistics.median(tg)
-    print(json.dumps({"mode": "qkv_fp8", "workload": w.name, "M": M, "N": N, "K": K,
+    timed = range(args.warmup, args.warmup + steps)
+    t_q = statistics.median(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in timed)
+    t_g = statistics.median(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in timed)
+    pk, src = peaks()
+    fp8_peak = 2 * pk["bf16_tflops"]  # the nominal fp8 : bf16 dense ratio applied to the measured bf16 burst
+    print(json.dumps({"mode": "qkv_fp8", "workload": w.name, "M": M, "N": N, "K": K, "steps": steps,
                       "quant_ms": t_q, "quant_GBps": 3 * M * K / t_q / 1e6,
-                      "gemm_ms": t_g, "gemm_TFLOPs": 2 * M * N * K / t_g / 1e9}))
+                      "gemm_ms": t_g, "gemm_TFLOPs": 2 * M * N * K / t_g / 1e9,
+                      "gemm_frac_of_fp8_peak": 2 * M * N * K / t_g / 1e9 / fp8_peak,
+                      "fp8_peak_TFLOPs": fp8_peak, "peak_source": src,
+                      "clocks": clocks.summary(wall0, wall1)}))
 
 
 def main():

@@ -16,13 +16,17 @@
 // on packed fp32 pairs) and converted with cvt.rn.satfinite.e4m3x2.  The codes
 // equal those of the IEEE quotient on every bf16 input (checked exhaustively).
 //
-// GEMM: persistent CTAs (one per SM) over 128 x 256 output tiles.  A TMA warp
-// streams 128-byte K blocks of A (128 rows) and B (256 rows) into a 4-stage
-// ring (128-byte swizzle) across tile boundaries; one thread issues
-// tcgen05.mma kind::f8f6f4 (M 128, N 256, K 32 per instruction) into one of two
-// 256-column fp32 TMEM accumulators; four epilogue warps drain the other: read
-// it back, apply the two scales, convert to bf16, stage 64-column boxes in two
-// alternating swizzled buffers and store them with TMA.  Waits are bounded.
+// GEMM: persistent CTA pairs (clusters of 2, one CTA per SM) over 256 x 256
+// output tiles.  Each CTA's TMA warp streams 128-byte K blocks of its 128 A
+// rows and of its half of the tile's 256 B rows into a 6-stage ring (128-byte
+// swizzle) across tile boundaries; one thread of the pair issues
+// tcgen05.mma.cta_group::2 kind::f8f6f4 (M 256, N 256, K 32 per instruction)
+// into one of two 256-column fp32 TMEM accumulators in each CTA; four epilogue
+// warps per CTA drain the other: read it back, apply the two scales, convert to
+// bf16, stage 64-column boxes in two alternating swizzled buffers and store
+// them with TMA.  Sharing B across the pair cuts each SM's operand loads from
+// 48 KB to 32 KB per 128-deep K block (one CTA per 128 x 256 tile: 3086 ->
+// 3440 TFLOP/s at the Wan2.2-480p QKV shape).  Waits are bounded.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -212,10 +216,14 @@ __global__ void __launch_bounds__(kQThreads) quant_fp8_rows_kernel(const uint4 *
 
 // ---------------------------------------------------------------- GEMM
 
-constexpr int kGM = 128, kGN = 256, kGK = 128;  // tile (K in bytes = elements)
-constexpr int kGStages = 4;
+// A CTA pair (cluster of 2) computes one 256 x 256 output tile: CTA r holds
+// rows 128 r .. 128 r + 127 of the tile's A block and columns 128 r .. + 127 of
+// its B block, and its own 128 x 256 fp32 accumulator in TMEM.
+constexpr int kGM = 128, kGN = 256, kGK = 128;  // per-CTA tile (K in bytes = elements)
+constexpr int kGBRows = kGN / 2;                // B rows (output columns) each CTA loads
+constexpr int kGStages = 6;  // 6 x 32 KB: ~2 us of MMA work buffered per SM
 constexpr int kGThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kABytes = kGM * kGK, kBBytes = kGN * kGK, kStageBytes = kABytes + kBBytes;
+constexpr int kABytes = kGM * kGK, kBBytes = kGBRows * kGK, kStageBytes = kABytes + kBBytes;
 constexpr int kOutBox = kGM * 128;                  // one output box: 128 rows x 64 bf16 columns
 constexpr int kOutOff = kGStages * kStageBytes;     // two output boxes, alternating
 constexpr int kBarOff = kOutOff + 2 * kOutBox;
@@ -231,21 +239,35 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
          | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// wait_bounded with cluster-scope acquire, for barriers the peer CTA arrives on.
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0 && (global_timer_ns() - t0 > kWaitLimitNs || i > kWaitLimitIters)) {
+      atomicOr(&g_fp8_error, 1u);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+// 2-D tiled load into this CTA's shared memory, counted on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster, int c0,
+                                                 int c1) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -261,10 +283,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Persistent: CTA c takes output tiles c, c + gridDim.x, ... (N fastest).  The
-// producer streams the K blocks of all its tiles through one ring; the MMA
-// thread accumulates tile i into TMEM buffer i % 2 and the epilogue warps drain
-// buffer i % 2 while the MMAs of tile i + 1 fill the other.
+// Persistent pairs: pair p takes 256 x 256 output tiles p, p + pairs, ... (N
+// fastest).  Both CTAs' producers stream their halves of each K block through
+// their own rings, completing on the rank-0 CTA's `full` barriers; one thread
+// of the rank-0 CTA issues the M = 256 MMAs (each CTA's A half and B half at
+// the same shared-memory offsets) and multicasts every commit to both CTAs; the
+// epilogue warps of each CTA drain its own accumulator rows and report the
+// buffer free on the rank-0 CTA's acc_empty (one arrive per warp).
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ a_scale,
@@ -274,9 +299,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + (base - raw) + kTmemSlotOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
   const int nk = (K + kGK - 1) / kGK;
   const int tiles_n = (N + kGN - 1) / kGN;
-  const int n_tiles = tiles_n * ((M + kGM - 1) / kGM);
+  const int n_tiles = tiles_n * ((M + 2 * kGM - 1) / (2 * kGM));
   const uint32_t bars = base + kBarOff;
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (kGStages + s); };
@@ -293,53 +320,63 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), 128);  // every epilogue thread, after its last TMEM read of the buffer
+      mbar_init(acc_empty(b), 8);  // one arrive per epilogue warp of both CTAs (rank 0's barrier counts)
     }
     mbar_init(drain, 1);
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(base + kTmemSlotOff, kGTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(base + kTmemSlotOff, kGTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before_sync();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive or load
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       uint32_t g = 0;  // K blocks issued over all tiles
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kGN;
+      for (int tile = pair; tile < n_tiles && ok; tile += pairs) {
+        const int m0 = (tile / tiles_n) * (2 * kGM) + static_cast<int>(rank) * kGM;
+        const int nb = (tile % tiles_n) * kGN + static_cast<int>(rank) * kGBRows;
         for (int kb = 0; kb < nk; ++kb, ++g) {
           const int s = g % kGStages;
           if (!wait_bounded(empty(s), ((g / kGStages) & 1) ^ 1)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full(s), kStageBytes);
-          tma_load_2d(base + s * kStageBytes, &tm_a, full(s), kb * kGK, m0);
-          tma_load_2d(base + s * kStageBytes + kABytes, &tm_b, full(s), kb * kGK, n0);
+          const uint32_t lead_full = mapa_shared(full(s), 0);
+          if (rank == 0) mbar_arrive_expect_tx(full(s), 2 * kStageBytes);
+          tma_load_2d_pair(base + s * kStageBytes, &tm_a, lead_full, kb * kGK, m0);
+          tma_load_2d_pair(base + s * kStageBytes + kABytes, &tm_b, lead_full, kb * kGK, nb);
         }
       }
-      // every copy issued must land before the CTA may exit
-      for (uint32_t i = g > kGStages ? g - kGStages : 0; i < g; ++i)
-        wait_bounded(full(i % kGStages), (i / kGStages) & 1);
+      // Copies must land before the CTA may exit.  Both CTAs' copies complete on
+      // rank 0's full barriers: rank 0 waits for the last fills there (the final
+      // cluster barrier keeps rank 1 resident until then); rank 1 sees its last
+      // fills consumed (their empty phase) on the normal path.
+      for (uint32_t i = g > kGStages ? g - kGStages : 0; i < g; ++i) {
+        if (rank == 0)
+          wait_bounded(full(i % kGStages), (i / kGStages) & 1);
+        else if (ok)
+          wait_bounded(empty(i % kGStages), (i / kGStages) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kGM, kGN);
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(2 * kGM, kGN);
       uint32_t g = 0;
       bool ok = true;
       int i = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++i) {
+      for (int tile = pair; tile < n_tiles && ok; tile += pairs, ++i) {
         const int buf = i & 1;
-        ok = wait_bounded(acc_empty(buf), ((i >> 1) & 1) ^ 1);  // the epilogue has drained this buffer
+        ok = wait_bounded_cluster(acc_empty(buf), ((i >> 1) & 1) ^ 1);  // both epilogues have drained it
         if (!ok) break;
         tc_fence_after_sync();
         const uint32_t d = tmem + buf * kGN;
@@ -351,30 +388,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
           const uint32_t a0 = base + s * kStageBytes, b0 = a0 + kABytes;
 #pragma unroll
           for (int kk = 0; kk < kGK / 32; ++kk)
-            mma_f8(d, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc,
-                   (kb > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(empty(s));
+            mma_f8_pair(d, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_pair(empty(s));
         }
-        if (ok) tc_commit(acc_full(buf));
+        if (ok) tc_commit_pair(acc_full(buf));
       }
-      // every MMA issued must complete before TMEM is freed
-      tc_commit(drain);
-      wait_bounded(drain, 0);
+      // every MMA issued must complete (in both CTAs) before TMEM is freed
+      tc_commit_pair(drain);
     }
+    if (lane == 0) wait_bounded(drain, 0);
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (both CTAs)
     // warp w reads TMEM lanes 32 * (w % 4) .. + 31: one output row per thread
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t sw = row & 7;
+    const uint32_t lead_acc_empty0 = mapa_shared(acc_empty(0), 0), lead_acc_empty1 = mapa_shared(acc_empty(1), 0);
     bool ok = true;
     int i = 0;
     int last_buf = -1;  // (row 0) staging buffer read by the most recently committed store
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
+    for (int tile = pair; tile < n_tiles; tile += pairs, ++i) {
       const int buf = i & 1;
-      const int m0 = (tile / tiles_n) * kGM, n0 = (tile % tiles_n) * kGN;
+      const int m0 = (tile / tiles_n) * (2 * kGM) + static_cast<int>(rank) * kGM, n0 = (tile % tiles_n) * kGN;
       ok = named_barrier_and(1, 128, ok && wait_bounded(acc_full(buf), (i >> 1) & 1));
       if (!ok) break;
       tc_fence_after_sync();
@@ -384,9 +422,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int box = c >> 1;  // 64 output columns per box, staged in buffer box % 2
         const uint32_t stage = base + kOutOff + (box & 1) * kOutBox;
         if ((c & 1) == 0) {
-          // every earlier store that reads this staging buffer must be done with it: all but the most
-          // recent store, or all of them if the most recent one reads this buffer too (boxes past N
-          // are skipped, so the buffers need not alternate between stores)
           if (row == 0) {
             if (last_buf == (box & 1))
               bulk_wait_read_all();
@@ -414,24 +449,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (c & 1) {
           fence_proxy_async_smem();
           named_barrier_sync(1, 128);
-          if (row == 0 && n0 + box * 64 < N) {
+          if (row == 0 && n0 + box * 64 < N && m0 < M) {
             tma_store_2d(&tm_o, stage, n0 + box * 64, m0);
             bulk_commit_group();
             last_buf = box & 1;
           }
         }
       }
-      // this thread's reads of the buffer are complete (each TMEM load waits): hand it back
+      // this warp's reads of the buffer are complete (each TMEM load waits): hand it back
       tc_fence_before_sync();
-      mbar_arrive(acc_empty(buf));
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(acc_empty(buf));
+        else
+          mbar_arrive_cluster(buf ? lead_acc_empty1 : lead_acc_empty0);
+      }
     }
     if (row == 0) bulk_wait_read_all();
   }
   tc_fence_before_sync();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs or loads may still touch it
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kGTmemCols);
+    tmem_dealloc_pair(tmem, kGTmemCols);
   }
 }
 
@@ -517,27 +559,50 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
                             const char **detail) {
   CUtensorMap ta, tb, to;
   if (!encode_2d(&ta, a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, M, lda, kGK, kGM) ||
-      !encode_2d(&tb, b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, ldb, kGK, kGN) ||
+      !encode_2d(&tb, b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, ldb, kGK, kGBRows) ||
       !encode_2d(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, M, ldo, 64, kGM)) {
     *detail = "cuTensorMapEncodeTiled failed for the fp8 GEMM operands";
     return cudaErrorInvalidValue;
   }
   static bool configured[64] = {};
+  static int max_pairs[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured[dev]) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kGThreads);
+  cfg.dynamicSmemBytes = kGSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     e = cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
     if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(sms & ~1);
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, gemm_fp8_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    max_pairs[dev] = clusters;
     configured[dev] = true;
   }
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + kGM - 1) / kGM);
-  const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);  // one persistent CTA per SM
-  return launch_kernel(gemm_fp8_kernel, dim3(grid), dim3(kGThreads), kGSmem, stream, ta, tb, to, a_scale, b_scale, M,
-                       N, K);
+  const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + 2 * kGM - 1) / (2 * kGM));
+  // persistent: as many pairs as can be resident at once (pairs wait only on each other)
+  const int pairs = static_cast<int>(tiles < max_pairs[dev] ? tiles : max_pairs[dev]);
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = launch_overlap_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel, ta, tb, to, a_scale, b_scale, M, N, K);
 }
 
 cudaError_t read_and_clear_fp8_error(unsigned int *value) {

@@ -582,7 +582,8 @@ def _fp8_operands(orc, M, N, K, seed, a_std=2.0, b_std=0.05):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 264, 208), (1, 8, 16), (520, 768, 1024),
-                                   (4100, 1288, 256)])  # the last: 198 tiles, so CTAs take two, ragged N
+                                   (4100, 1288, 256)])  # the last: 102 tiles of 256 x 256, so CTA pairs take two,
+# ragged N; M = 1 and 300 leave the second CTA of a pair rows wholly past M
 def test_gemm_fp8_parity(orc, M, N, K):
     (a, sa, b, sb), (da, dsa, db, dsb) = _fp8_operands(orc, M, N, K, seed=M + 3 * N + K)
     out = ops.gemm_fp8(da, dsa, db, dsb)
@@ -603,7 +604,8 @@ def test_gemm_fp8_strided_output(orc):
 
 def test_gemm_fp8_qkv_projection_full_size(orc):
     """The Qwen-Image-Edit QKV projection (17248 tokens x 9216 x 3072) in the launch bench.py times: every CTA
-    runs 32 tiles; sampled output rows against the oracle."""
+    pair runs 32 or 33 tiles of 256 x 256, the last tile row holds 96 tokens; sampled output rows against the
+    oracle."""
     M, N, K = 17248, 9216, 3072
     # any e4m3 codes are valid GEMM operands: seeded random bytes (NaN codes replaced) and scales
     rng = np.random.default_rng(97)
