@@ -618,6 +618,7 @@ def run_ours(args):
                # the spread of the steps (the host link is shared with the machine's other GPUs)
                "ms_per_step_min": min(ts_e2e) * 1e3, "ms_per_step_median": statistics.median(ts_e2e) * 1e3,
                "ms_per_step_max": max(ts_e2e) * 1e3,
+               "ms_each": [round(t * 1e3, 1) for t in ts_e2e],
                "host_to_device_GBps": h2d_gbps,
                "host_call_ms_median": statistics.median(host) * 1e3, "host_call_ms_max": max(host) * 1e3,
                "api": "dit_attention_host (" + ("query ranges, stacked partials + merge kernel per range, each "
