@@ -56,6 +56,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "attn_math.cuh"
@@ -599,12 +600,12 @@ cudaError_t launch_typed(const CUtensorMap &tq, const CUtensorMap &tk, const CUt
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool configured[64] = {};
-  if (dev < 64 && !configured[dev]) {
+  static std::atomic<bool> configured[64];  // set once the attribute is (other host threads may launch too)
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D, kCausal, kUpdate>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay::kAlloc);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   dim3 grid((a.Sq + kBM * kNQ - 1) / (kBM * kNQ), a.H, B);
   return launch_kernel(attn_fwd_kernel<D, kCausal, kUpdate>, grid, dim3(kThreads), Lay::kAlloc, stream, tq, tk, tv,

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <atomic>
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -282,15 +283,15 @@ template <typename Tin, typename Tout, int C>
 cudaError_t launch_bulk(const void *o_parts, const float *lse_parts, int B, int H, int Sq, long long pso,
                         long long psl, void *o, float *lse, cudaStream_t stream) {
   constexpr int D = 128;
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // set once the attribute is (other host threads may launch too)
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(merge_lse_bulk_kernel<Tin, Tout, D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kBulkSmem);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;

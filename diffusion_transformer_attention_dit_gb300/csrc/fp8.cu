@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "attn_math.cuh"
@@ -564,8 +565,8 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
     *detail = "cuTensorMapEncodeTiled failed for the fp8 GEMM operands";
     return cudaErrorInvalidValue;
   }
-  static bool configured[64] = {};
-  static int max_pairs[64] = {};
+  // pairs that can be resident at once, per device (0: not yet known); other host threads may launch too
+  static std::atomic<int> max_pairs[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -581,8 +582,8 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
   cfg.dynamicSmemBytes = kGSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  if (dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  int cap = dev < 64 ? max_pairs[dev].load(std::memory_order_acquire) : 0;
+  if (cap == 0) {
     e = cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
     if (e != cudaSuccess) return e;
     int sms = 0;
@@ -590,16 +591,14 @@ cudaError_t launch_gemm_fp8(const void *a, const float *a_scale, const void *b, 
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(sms & ~1);
     cfg.numAttrs = 1;
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, gemm_fp8_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&cap, gemm_fp8_kernel, &cfg);
     if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    max_pairs[dev] = clusters;
-    configured[dev] = true;
+    if (cap < 1) return cudaErrorInvalidConfiguration;
+    if (dev < 64) max_pairs[dev].store(cap, std::memory_order_release);
   }
   const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + 2 * kGM - 1) / (2 * kGM));
   // persistent: as many pairs as can be resident at once (pairs wait only on each other)
-  const int pairs = static_cast<int>(tiles < max_pairs[dev] ? tiles : max_pairs[dev]);
+  const int pairs = static_cast<int>(tiles < cap ? tiles : cap);
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = launch_overlap_enabled() ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel, ta, tb, to, a_scale, b_scale, M, N, K);

@@ -21,6 +21,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "sm100_ptx.cuh"
 
@@ -191,14 +193,14 @@ template <int D>
 cudaError_t launch_typed(const void *q, const void *k, void *q_out, void *k_out, const float *wq, const float *wk,
                          const float *cos_tab, const float *sin_tab, int S, int H, float eps, long long n_rows,
                          cudaStream_t stream) {
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // set once the attribute is (other host threads may launch too)
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(qk_norm_rope_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    if (dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
