@@ -25,7 +25,7 @@
 // and writes two rows, loading each thread's scale / shift vectors once for
 // both -- those per-row factor reads (twice the row's own bytes, through L1)
 // are what held the one-row kernel at 0.84 of the measured HBM bandwidth at
-// the Wan2.2 720p shape; two rows a step run at 0.89.  (Also measured on GB300
+// the Wan2.2 720p shape; two rows a step run at 0.92.  (Also measured on GB300
 // and slower: three rows a step, the next pair prefetched, deeper prefetch in
 // registers or a ring of rows in shared memory filled by cp.async or by bulk
 // copies, one warp per row, and fewer CTAs per SM.)
@@ -286,8 +286,16 @@ __device__ __forceinline__ void process_pair(const uint4 (&ra)[kVec], uint32_t f
 // that pays for it), the other CTAs on the SM keep HBM busy meanwhile.
 // Loading each factor vector once per pair halves the factor reads that
 // bound the one-row kernel.
+// Residency targets of the two-row kernel (CTAs per SM, i.e. a register cap of
+// 65536 / (128 x target)).  Left to itself the compiler gives 4-5 vectors per
+// thread 92-96 registers, 5 CTAs per SM; capped at 80 (no spills there) they
+// run 6, which measured faster (Wan2.2 shapes, C = 5120: 0.89 -> 0.92 of HBM).
+// The other widths keep the residency they get uncapped (56-116 registers);
+// a 6 there would lower it (1-3 vectors) or spill (6-7).
+constexpr int pair_min_blocks(int vec) { return vec <= 2 ? 8 : vec == 3 ? 7 : vec <= 5 ? 6 : vec == 6 ? 5 : 4; }
+
 template <int kVec>
-__global__ void __launch_bounds__(kThreads) row_pair_kernel(const uint4 *__restrict__ x, uint8_t *y,
+__global__ void __launch_bounds__(kThreads, pair_min_blocks(kVec)) row_pair_kernel(const uint4 *__restrict__ x, uint8_t *y,
                                                             const float *__restrict__ a,
                                                             const float *__restrict__ c, long long rows, int C,
                                                             int L, float eps) {
