@@ -20,7 +20,9 @@
 // FFMA2 / FMUL2).
 //
 // Two kernels.  The one-row kernel (RMSNorm; LayerNorm at C = 8192): persistent
-// CTAs issue the next row's loads before reducing the current one.  The
+// CTAs issue the next row's loads before reducing the current one (RMSNorm at
+// C = 5120 with a 7-CTA residency target: 0.95 of the measured HBM bandwidth
+// at the Wan2.2 720p shape).  The
 // two-row kernel (LayerNorm-modulate up to C = 7168): a step loads, reduces
 // and writes two rows, loading each thread's scale / shift vectors once for
 // both -- those per-row factor reads (twice the row's own bytes, through L1)
@@ -202,9 +204,8 @@ __device__ __forceinline__ void load_row(uint4 (&raw)[kVec], uint32_t &first, co
 // are in flight.  One barrier per row: consecutive rows alternate between
 // red[0..7] and red[8..15].
 template <int kMode, int kVec>
-__global__ void __launch_bounds__(kThreads) row_kernel(const uint4 *__restrict__ x, uint8_t *y,
-                                                       const float *__restrict__ a, const float *__restrict__ c,
-                                                       long long rows, int C, int L, float eps) {
+__device__ __forceinline__ void row_loop(const uint4 *__restrict__ x, uint8_t *y, const float *__restrict__ a,
+                                         const float *__restrict__ c, long long rows, int C, int L, float eps) {
   __shared__ float red[16];
   const int nvec = C / 8;
   uint4 cur[kVec], nxt[kVec];
@@ -222,6 +223,26 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const uint4 *__restrict__
     if (r2 < rows) load_row<kVec>(cur, fcur, x, r2, nvec);
     process_row<kMode, kVec>(nxt, fnxt, y, a, c, r1, nvec, C, L, eps, red + 8);
   }
+}
+
+template <int kMode, int kVec>
+__global__ void __launch_bounds__(kThreads) row_kernel(const uint4 *__restrict__ x, uint8_t *y,
+                                                       const float *__restrict__ a, const float *__restrict__ c,
+                                                       long long rows, int C, int L, float eps) {
+  row_loop<kMode, kVec>(x, y, a, c, rows, C, L, eps);
+}
+
+// The same with a residency target of 7 CTAs per SM (registers capped at 72).
+// RMSNorm at 5 vectors per thread (C = 4097 ... 5120) measured faster so
+// (68 registers, 7 CTAs, against the compiler's 64 registers and 8 CTAs): the
+// Wan2.2 shapes 0.92 -> 0.95 (720p) and 0.89 -> 0.90 (480p) of HBM.  At 4
+// vectors the same target was slower, and at 6-8 it spills.
+template <int kMode, int kVec>
+__global__ void __launch_bounds__(kThreads, 7) row_kernel_res7(const uint4 *__restrict__ x, uint8_t *y,
+                                                               const float *__restrict__ a,
+                                                               const float *__restrict__ c, long long rows, int C,
+                                                               int L, float eps) {
+  row_loop<kMode, kVec>(x, y, a, c, rows, C, L, eps);
 }
 
 // Sums of four values over the CTA, as block_reduce2 (`red` holds 16 floats).
@@ -340,6 +361,8 @@ cudaError_t launch_vec(const void *x, void *y, const float *a, const float *c, l
                        int L, float eps, cudaStream_t stream) {
   if constexpr (kMode == kLayerNormModulate && kVec <= 7)
     return launch_persistent(row_pair_kernel<kVec>, (rows + 1) / 2, x, y, a, c, rows, C, L, eps, stream);
+  else if constexpr (kMode == kRmsNorm && kVec == 5)
+    return launch_persistent(row_kernel_res7<kMode, kVec>, rows, x, y, a, c, rows, C, L, eps, stream);
   else
     return launch_persistent(row_kernel<kMode, kVec>, rows, x, y, a, c, rows, C, L, eps, stream);
 }
