@@ -62,7 +62,7 @@ MERGE = {"tiny": "update", "qwen_image": "update", "qwen_image_edit": "update", 
 PER_WORKLOAD = ("qwen_image", "qwen_image_edit", "wan480")
 # DRAM bytes (read + write) per attention launch, from an ncu capture of the attention kernel whose code (source
 # without comments, attn_source_digest) has this sha256 prefix; reported as roofline.traffic only while it matches.
-ATTN_TRAFFIC = {"source_sha256_prefix": "d890e333cbc9a932", "by_workload": {"wan720": 1717.5e6},
+ATTN_TRAFFIC = {"source_sha256_prefix": "4f9d9b792e932a0e", "by_workload": {"wan720": 1716.6e6},
                 "capture": "stored ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of one Wan2.2-720p "
                            "chunk launch, bench.py --profile-kernel attention --workload wan720"}
 
