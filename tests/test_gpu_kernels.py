@@ -602,13 +602,13 @@ def test_gemm_fp8_strided_output(orc):
     assert torch.count_nonzero(buf[:, N:]) == 0
 
 
-def test_gemm_fp8_qkv_projection_full_size(orc):
-    """The Qwen-Image-Edit QKV projection (17248 tokens x 9216 x 3072) in the launch bench.py times: every CTA
-    pair runs 32 or 33 tiles of 256 x 256, the last tile row holds 96 tokens; sampled output rows against the
-    oracle."""
-    M, N, K = 17248, 9216, 3072
+@pytest.mark.parametrize("M,N,K", [(17248, 9216, 3072), (32760, 15360, 5120)])
+def test_gemm_fp8_qkv_projection_full_size(orc, M, N, K):
+    """The QKV projections of Qwen-Image-Edit (17248 tokens x 9216 x 3072) and Wan2.2 480p (32760 x 15360 x
+    5120) in the launch bench.py times: every CTA pair runs 32-33 (Edit) or 101-102 (Wan480) tiles of 256 x
+    256, and the last tile row holds 96 or 248 tokens; sampled output rows against the oracle."""
     # any e4m3 codes are valid GEMM operands: seeded random bytes (NaN codes replaced) and scales
-    rng = np.random.default_rng(97)
+    rng = np.random.default_rng(97 + K)
     a = rng.integers(0, 256, (M, K), dtype=np.uint8)
     b = rng.integers(0, 256, (N, K), dtype=np.uint8)
     a[(a & 0x7F) == 0x7F] = 0x38
