@@ -12,10 +12,13 @@ LSE-merge kernel.
 The JSON line (rank 0) carries, beside the step throughput:
   roofline      the attention launches of the step, timed in a second region of
                 the same steps (events around the attention launches only)
-  hbm           the step's merge kernel (events around it in that region) and
-                the QK-RMSNorm + RoPE prologue at the workload's shapes, timed
-                alone; algorithmic bytes / time against the measured HBM copy
-                bandwidth
+  hbm           the step's merge kernel (events around it in that region) and,
+                timed alone at the workload's shapes, the QK-RMSNorm + RoPE
+                prologue and the DiT block's LayerNorm-modulate, RMSNorm over
+                C and fp8 quantiser on its tokens; algorithmic bytes / time
+                against the measured HBM copy bandwidth
+  fp8_gemm      the W8A8 QKV projection of those tokens (tcgen05 fp8 GEMM),
+                timed alone, against 2x the measured bf16 peaks
   per_workload  the other full-size workloads (Qwen-Image, Qwen-Image-Edit,
                 Wan2.2 480p), each its own step and attention regions
   e2e           the public host-buffer call (dit_attention_host) with the
@@ -430,15 +433,14 @@ def time_workload(ds, steps, uuid, world=1):
     return res
 
 
-def time_prologue_alone(ds, uuid, seconds: float = REGION_S):
-    """The prologue kernel alone at the workload's shapes (L2 flushed before every launch), for about `seconds`."""
+def time_alone(run, flush, uuid, seconds: float = REGION_S):
+    """One kernel launched alone, back to back for about `seconds` with L2 flushed before every launch; median
+    seconds per launch, the launch count and the clock record."""
     import torch
 
     from diffusion_transformer_attention_dit_gb300 import ops
 
     stream = torch.cuda.current_stream()
-    qo, ko = torch.empty_like(ds.q), torch.empty_like(ds.k)
-    run = lambda: ops.qk_norm_rope(ds.q, ds.k, *ds.tabs, ds.w.eps, q_out=qo, k_out=ko)  # noqa: E731
     for _ in range(3):
         run()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -453,7 +455,7 @@ def time_prologue_alone(ds, uuid, seconds: float = REGION_S):
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for i in range(n):
-            ds.flush.zero_()
+            flush.zero_()
             ev[2 * i].record(stream)
             run()
             ev[2 * i + 1].record(stream)
@@ -461,8 +463,73 @@ def time_prologue_alone(ds, uuid, seconds: float = REGION_S):
         wall1 = time.perf_counter()
     ops.poll_device_error()
     ts = [ev[2 * i].elapsed_time(ev[2 * i + 1]) / 1e3 for i in range(n)]
-    del qo, ko
     return statistics.median(ts), n, clocks.summary(wall0, wall1)
+
+
+def time_prologue_alone(ds, uuid, seconds: float = REGION_S):
+    """The prologue kernel alone at the workload's shapes (L2 flushed before every launch), for about `seconds`."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import ops
+
+    qo, ko = torch.empty_like(ds.q), torch.empty_like(ds.k)
+    out = time_alone(lambda: ops.qk_norm_rope(ds.q, ds.k, *ds.tabs, ds.w.eps, q_out=qo, k_out=ko), ds.flush, uuid,
+                     seconds)
+    del qo, ko
+    return out
+
+
+def block_kernel_records(ds, uuid, pk):
+    """The DiT block's other kernels on this workload's tokens, each alone (L2 flushed before every launch, a
+    ~REGION_S region with its clock record): LayerNorm-modulate, RMSNorm over C and the fp8 quantiser on the
+    tokens as [B*S, C = H*D] rows (x = the workload's q), and the fp8 QKV projection GEMM they feed
+    ([B*S, C] x [3C, C] codes).  Returns (hbm records, the GEMM record)."""
+    import torch
+
+    from diffusion_transformer_attention_dit_gb300 import ops
+
+    w = ds.w
+    B, S, C = w.B, w.S, w.H * w.D
+    M = B * S
+    dev = ds.q.device
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242 + w.index)
+    x = ds.q.view(B, S, C)
+    sc = 0.1 * torch.randn(B, C, device=dev, generator=g)
+    sh = 0.1 * torch.randn(B, C, device=dev, generator=g)
+    wn = 1 + 0.1 * torch.randn(C, device=dev, generator=g)
+    y = torch.empty_like(x)
+    codes = torch.empty((M, C), dtype=torch.uint8, device=dev)
+    scale = torch.empty(M, dtype=torch.float32, device=dev)
+    hbm = {}
+    how = (f"the kernel alone on this workload's tokens as [{M}, {C}] bf16 rows (x = the workload's q), L2 "
+           "flushed before every launch, median")
+    t, n, clk = time_alone(lambda: ops.layer_norm_modulate(x, sc, sh, w.eps, y=y), ds.flush, uuid)
+    hbm["layer_norm_modulate"] = hbm_record("row_pair_kernel (LayerNorm-modulate)", t, 4 * M * C + 8 * B * C,
+                                            pk["hbm_gbs"], n, clk, how + "; fp32 scale / shift per batch entry")
+    t, n, clk = time_alone(lambda: ops.rms_norm(x, wn, w.eps, y=y), ds.flush, uuid)
+    hbm["rms_norm"] = hbm_record("row_kernel (RMSNorm over C)", t, 4 * M * C + 4 * C, pk["hbm_gbs"], n, clk, how)
+    t, n, clk = time_alone(lambda: ops.quant_fp8_rows(x.view(M, C), codes, scale), ds.flush, uuid)
+    hbm["quant_fp8_rows"] = hbm_record("quant_fp8_rows_kernel", t, 3 * M * C + 4 * M, pk["hbm_gbs"], n, clk,
+                                       how + "; e4m3 codes and a per-row scale out")
+    del y
+    wt = (0.02 * torch.randn(3 * C, C, device=dev, generator=g)).to(torch.bfloat16)
+    wq, ws = ops.quant_fp8_rows(wt)
+    del wt
+    out = torch.empty((M, 3 * C), dtype=torch.bfloat16, device=dev)
+    t, n, clk = time_alone(lambda: ops.gemm_fp8(codes, scale, wq, ws, out=out), ds.flush, uuid)
+    flops = 2.0 * M * 3 * C * C
+    tf = flops / t / 1e12
+    peak, peak_s = 2 * pk["bf16_tflops"], 2 * pk["bf16_tflops_sustained"]
+    gemm = {"kernel": "gemm_fp8_kernel (CTA pairs)", "M": M, "N": 3 * C, "K": C, "flops": flops, "us": t * 1e6,
+            "TFLOP/s": tf, "peak": peak, "frac": tf / peak, "peak_sustained": peak_s, "frac_sustained": tf / peak_s,
+            "peak_kind": "2x the measured bf16 burst / sustained figures (the nominal fp8 : bf16 dense ratio)",
+            "launches": n, "timing": "the W8A8 QKV projection of these tokens alone ([M, K] x [N, K] e4m3 codes, "
+                                     "per-row / per-channel scales, bf16 out), L2 flushed before every launch, "
+                                     "median", "clocks": clk}
+    del out, codes, scale, wq, ws
+    torch.cuda.empty_cache()
+    return hbm, gemm
 
 
 def hbm_record(name, t_s, nbytes, peak_gbs, launches, clocks, how):
@@ -606,6 +673,10 @@ def run_ours(args):
             "qk_norm_rope_kernel", t_pro, prologue_bytes(B, S, H, D), pk["hbm_gbs"], n_pro, clk_pro,
             f"the prologue kernel alone on this workload's q, k, weights and rotary tables (the step "
             f"{'runs it' if w.prologue else 'has none'}), L2 flushed before every launch, median")
+    fp8_gemm = None
+    if not args.no_hbm and not args.no_block_kernels:
+        more, fp8_gemm = block_kernel_records(ds, uuid, pk)
+        hbm.update(more)
 
     e2e = None
     if not args.no_e2e:
@@ -656,6 +727,7 @@ def run_ours(args):
                                    "the last attention launch (the step region carries no events between kernels)",
                          "clocks": r["clocks_attn"]},
             "hbm": hbm,
+            "fp8_gemm": fp8_gemm,
             "per_workload": per,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -952,7 +1024,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true", help="skip the per_workload record")
-    ap.add_argument("--no-hbm", action="store_true", help="skip the prologue-alone entry of the hbm record")
+    ap.add_argument("--no-hbm", action="store_true", help="skip the kernels timed alone (prologue, block kernels, fp8 GEMM)")
+    ap.add_argument("--no-block-kernels", action="store_true",
+                    help="skip the LayerNorm-modulate / RMSNorm / quantiser entries of the hbm record and the fp8 GEMM")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--ring-overlap", type=int, default=0, metavar="RANKS",
                     help="time the one-GPU ring-overlap emulation with RANKS key shards instead (diagnostic)")

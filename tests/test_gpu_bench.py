@@ -29,7 +29,11 @@ def test_bench_line_has_every_field():
     roof = line["roofline"]
     assert roof["bound"] == "tensor" and roof["achieved"] > 0 and roof["peak"] > 0
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
-    assert "qk_norm_rope" in line["hbm"] and line["hbm"]["qk_norm_rope"]["GB/s"] > 0
+    for k in ("qk_norm_rope", "layer_norm_modulate", "rms_norm", "quant_fp8_rows"):
+        assert k in line["hbm"] and line["hbm"][k]["GB/s"] > 0 and "clocks" in line["hbm"][k], k
+    gemm = line["fp8_gemm"]
+    assert gemm["TFLOP/s"] > 0 and abs(gemm["frac"] - gemm["TFLOP/s"] / gemm["peak"]) < 1e-9
+    assert (gemm["M"], gemm["N"], gemm["K"]) == (256, 384, 128)  # tiny: 256 tokens, C = H * D = 128
     e2e = line["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert "dit_attention_host" in e2e["api"]
