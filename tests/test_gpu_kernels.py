@@ -459,7 +459,8 @@ def test_attn_fwd_causal_chunks_merge(orc):
 # every CTA several pairs; C = 7168 is the widest row of the two-row kernel,
 # C = 8192 the one-row kernel's
 @pytest.mark.parametrize("B,L,C", [(2, 37, 3072), (1, 130, 5120), (3, 5, 8), (1, 7, 8192), (2, 300, 128),
-                                   (3, 3, 7168), (3, 1001, 1024), (2, 2049, 5120), (2, 65, 4096), (1, 33, 6144)])
+                                   (3, 3, 7168), (3, 1001, 1024), (2, 2049, 5120), (2, 65, 4096), (1, 33, 6144),
+                                   (4, 1, 512), (1, 1, 256)])  # every pair straddles; one row
 def test_layer_norm_modulate_parity(orc, B, L, C):
     rng = np.random.default_rng(C + L)
     x = inputs.bf16_normal(B * L * C, seed=C + 7, std=2.0, mean=0.3).reshape(B, L, C)
